@@ -1,0 +1,451 @@
+"""Benchmark of the fused fp16 GEMM + ReLU hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. the fused kernel on M = N = K = 4096 (A, B ~ N(0,1)/sqrt(K)): tile
+     rasteriser, TMA ring, tcgen05 MMA into TMEM, ReLU/fp16 epilogue;
+  2. the split-K kernel on M = 16, N = K = 8192 (N(0,1)/sqrt(K)), split 8:
+     partials to the workspace, last-arriver reduction with ReLU.
+Metric: GEMM+ReLU TFLOP/s = total 2*M*N*K of the step / step time.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs the same step on its own GPU
+(independent replicas, weak scaling); rank 0 prints one JSON line.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp16 and bf16 dense tensor rates are the same on this architecture (2.25
+# PFLOP/s nominal each), so the measured bf16 peak is the fp16 denominator.
+FP16_PER_BF16 = 1.0
+L2_FLUSH_BYTES = 512 << 20
+
+METRIC = "GEMM+ReLU TFLOP/s (fp16 in, fp32 acc)"
+
+# DRAM bytes (read + write) per launch from ncu captures of the current
+# kernels, keyed by (kind, M, N, K); a shape missing here reports null.
+DRAM_BYTES_PER_LAUNCH = {}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ workload
+
+STEP_NAME = ("square4096 fused (M=N=K=4096, N(0,1)/sqrt(K)) + skinny split-K "
+             "(M=16, N=K=8192, N(0,1)/sqrt(K), split 8)")
+
+
+def describe(w):
+    dist = {"normal": "N(0,1)", "uniform": "U[-1,1]"}[w.dist] + ("/sqrt(K)" if w.scale_by_sqrt_k else "")
+    s = f"{w.name} (M={w.M}, N={w.N}, K={w.K}, {dist}"
+    return s + (f", split-K {w.split_k})" if w.split_k > 1 else ")")
+
+
+def build_parts(args):
+    """[(label, workload, kind)], description.  kind: 'fused' or 'splitk'."""
+    from tiled_tensor_core_03_gb300 import inputs
+    W = inputs.WORKLOADS
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.lower().split("x"))
+        w = inputs.Workload("custom", M, N, K, "normal", True, 7, split_k=args.split)
+        return [("custom", w, "splitk" if args.split > 1 else "fused")], describe(w)
+    if args.workload == "step":
+        return [("fused_4096", W["square4096"], "fused"),
+                ("splitk_skinny", W["skinny"], "splitk")], STEP_NAME
+    w = W[args.workload]
+    return [(w.name, w, "splitk" if w.split_k > 1 else "fused")], describe(w)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=5)
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((t, parts))
+        lo = (self.t_start or 0) - 0.15
+        hi = (self.t_end or 1e30) + 0.15
+        window = [r for r in rows if lo <= r[0] <= hi] or rows[-3:]
+        sm = [float(p[2]) for _, p in window if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for _, p in window if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in window for i in range(4)
+                          if p[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(window)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_rows_sample(parts, host_inputs, budget_s, min_rows=1):
+    """Time the CPU oracle (single thread, as it stands) on a bounded sample of
+    the step: whole output rows of each part's problem, taken in proportion to
+    the part's share of the step's FLOPs, until `budget_s` seconds of oracle
+    time are spent.  Returns (flops, seconds, {label: (rows, output)})."""
+    import oracle
+    orc = oracle.Oracle()
+    total = sum(w.flops for _, w, _ in parts)
+    done = {label: 0 for label, _, _ in parts}
+    flops = {label: 0 for label, _, _ in parts}
+    outs = {label: [] for label, _, _ in parts}
+    elapsed = 0.0
+    while True:
+        # the part furthest behind its share of the step's FLOPs
+        label, w, _ = min(parts, key=lambda p: flops[p[0]] / (p[1].flops / total))
+        if done[label] >= w.M:
+            break
+        A, B = host_inputs[label]
+        t0 = time.perf_counter()
+        outs[label].append(orc.gemm_relu_f16_rows(A, B, done[label], 1))
+        elapsed += time.perf_counter() - t0
+        done[label] += 1
+        flops[label] += 2 * w.N * w.K
+        if elapsed >= budget_s and all(done[l] >= min_rows for l in done):
+            break
+    out = {l: (done[l], np.concatenate(outs[l]) if outs[l] else None) for l in done}
+    return sum(flops.values()), elapsed, out
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value, world, device=None):
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, timed on the host, each
+    step a bounded sample (whole output rows) of the same workload."""
+    if rank != 0:
+        return 0
+    import multiprocessing
+    from tiled_tensor_core_03_gb300 import inputs
+    parts, name = build_parts(args)
+    host_inputs = {label: inputs.make_workload(w) for label, w, _ in parts}
+    budget = min(2.0, 150.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rows_sample(parts, host_inputs, budget * 0.25)
+    flops, secs = 0, 0.0
+    for _ in range(args.steps):
+        f, dt, _ = oracle_rows_sample(parts, host_inputs, budget)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": name, "parallelism": f"replicas{args.gpus}"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step, whole output rows of each problem in proportion "
+                                   f"to its FLOP share, about {budget:.2f} s of single-threaded "
+                                   f"fp64 C oracle time; host has {multiprocessing.cpu_count()} cores"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+    import tiled_tensor_core_03_gb300 as gr
+    from tiled_tensor_core_03_gb300 import _build, inputs
+
+    if _build.needs_build():
+        _build.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    parts, name = build_parts(args)
+    host_inputs = {label: inputs.make_workload(w) for label, w, _ in parts}
+    dev = {}
+    for label, w, kind in parts:
+        A, B = host_inputs[label]
+        a = torch.from_numpy(A).to(device)
+        b = torch.from_numpy(B).to(device)
+        c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+        ws = gr.splitk_workspace(w.M, w.N, w.K, w.split_k, device) if kind == "splitk" else None
+        dev[label] = (a, b, c, ws)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def launch(label, w, kind):
+        a, b, c, ws = dev[label]
+        if kind == "splitk":
+            gr.gemm_relu_splitk(a, b, w.split_k, out=c, workspace=ws, stream=stream)
+        else:
+            gr.gemm_relu(a, b, out=c, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        for p in parts:
+            launch(*p)
+    torch.cuda.synchronize(device)
+    st = gr.status(stream)
+    if st != gr.OK:
+        raise RuntimeError(f"device status after warm-up: {gr.strerror(st)}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)]
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    sampler.mark("t_start")
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                    # L2 flush between steps, outside the events
+        ev[i][0].record(stream)
+        for j, p in enumerate(parts):
+            launch(*p)
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.perf_counter()
+    sampler.mark("t_end")
+    barrier(world)
+    sampler.stop()
+    st = gr.status(stream)
+    if st != gr.OK:
+        raise RuntimeError(f"device status after timed steps: {gr.strerror(st)}")
+
+    part_ms = {label: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
+               for j, (label, _, _) in enumerate(parts)}
+    step_ms_local = sum(sum(v) for v in part_ms.values()) / args.steps
+    step_ms = max_over_ranks(step_ms_local, world, device)
+    flops_step = sum(w.flops for _, w, _ in parts)
+    value = world * flops_step / (step_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API, host buffers in pinned memory
+    pinned = {}
+    for label, w, _ in parts:
+        A, B = host_inputs[label]
+        pinned[label] = (torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(),
+                         torch.empty((w.M, w.N), dtype=torch.float16).pin_memory())
+
+    def e2e_step():
+        for label, w, kind in parts:
+            hA, hB, hC = pinned[label]
+            a, b, c, _ = dev[label]
+            a.copy_(hA, non_blocking=True)
+            b.copy_(hB, non_blocking=True)
+            launch(label, w, kind)
+            hC.copy_(c, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, world, device)
+    barrier(world)
+    h2d = sum(2 * (w.M * w.K + w.K * w.N) for _, w, _ in parts)
+    d2h = sum(2 * w.M * w.N for _, w, _ in parts)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks, peaks_src = load_peaks()
+    tensor_peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP16_PER_BF16
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
+
+    def roofline(label, w, kind):
+        ms = statistics.mean(part_ms[label])
+        kernel = (f"gemm_relu_splitk_kernel {w.M}x{w.N}x{w.K} split {w.split_k}"
+                  if kind == "splitk" else f"gemm_relu_fused_kernel {w.M}x{w.N}x{w.K}")
+        if w.flops / w.bytes >= ridge:
+            ach = w.flops / (ms * 1e-3) / 1e12
+            return {"bound": "tensor", "kernel": kernel, "achieved": ach, "peak": tensor_peak,
+                    "unit": "TFLOP/s", "frac": ach / tensor_peak, "ms": ms,
+                    "algorithmic_flops": w.flops,
+                    "peak_source": f"{peaks_src} bf16_tflops (burst) x {FP16_PER_BF16} (fp16/bf16)",
+                    "traffic": DRAM_BYTES_PER_LAUNCH.get((kind, w.M, w.N, w.K))}
+        ach = w.bytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": kernel, "achieved": ach, "peak": hbm_peak,
+                "unit": "GB/s", "frac": ach / hbm_peak, "ms": ms, "algorithmic_bytes": w.bytes,
+                "peak_source": f"{peaks_src} hbm_gbs",
+                "traffic": DRAM_BYTES_PER_LAUNCH.get((kind, w.M, w.N, w.K))}
+
+    roofs = {label: roofline(label, w, kind) for label, w, kind in parts}
+    dominant = max(parts, key=lambda p: sum(part_ms[p[0]]))[0]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": name,
+            "flops_per_step": flops_step,
+            "parallelism": f"replicas{world}",
+            "l2": f"flushed between steps by a {L2_FLUSH_BYTES >> 20} MiB write (outside the events)",
+            "timing": "CUDA events around each launch on the launching stream, summed per step",
+        },
+        "roofline": roofs[dominant],
+        "parts": {label: {"ms": statistics.mean(part_ms[label]),
+                          "tflops": w.flops / (statistics.mean(part_ms[label]) * 1e-3) / 1e12,
+                          "gbs": w.bytes / (statistics.mean(part_ms[label]) * 1e-3) / 1e9,
+                          "roofline": roofs[label]}
+                  for label, w, _ in parts},
+        "wall_ms_per_step_incl_flush": 1e3 * (wall1 - wall0) / args.steps,
+        "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "tiled_tensor_core_03_gb300.gemm_relu / gemm_relu_splitk from pinned host buffers"},
+        "gpu_launches": len(parts) * args.steps,
+        "clocks": sampler.summary(),
+    }
+
+    if world == 1 and not args.no_cpu_baseline:
+        import multiprocessing
+        f, dt, outs = oracle_rows_sample(parts, host_inputs, args.cpu_budget)
+        err = 0.0
+        for label, (rows, want) in outs.items():
+            if rows:
+                got = dev[label][2][:rows].cpu().numpy().astype(np.float64)
+                err = max(err, float(np.abs(got - want.astype(np.float64)).max()))
+        desc = ", ".join(f"first {rows} rows of {label}" for label, (rows, _) in outs.items())
+        line["cpu_baseline"] = {
+            "value": f / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{desc} ({f / 1e9:.2f} GFLOP in {dt:.1f} s), single-threaded fp64 C "
+                      f"oracle; host has {multiprocessing.cpu_count()} cores",
+            "max_abs_err_vs_gpu_on_sample": err,
+        }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--workload", default="step",
+                    choices=["step", "square256", "square1024", "ragged", "square4096", "skinny"])
+    ap.add_argument("--shape", default=None, help="MxNxK: one custom fused (or split) GEMM")
+    ap.add_argument("--split", type=int, default=1, help="split-K for --shape")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,151 @@
+/*
+ * gemm_relu.h -- C ABI of libgemmrelu.so: fused fp16 GEMM + ReLU on GB300 (sm_103a).
+ *
+ *     C = fp16( max( A . B , 0 ) )
+ *
+ * A is M x K, B is K x N, C is M x N; all three are dense, row-major fp16
+ * (leading dimensions K, N and N).  Products accumulate in fp32 inside the
+ * tensor cores; ReLU is applied to the fp32 accumulator and the result is
+ * rounded to fp16 (round-to-nearest-even) once, on the way out.
+ *
+ * The operation is the one defined by the FP16 GEMM + ReLU quickstart of
+ * "TileLang 编程基本知识点" (section 二: fp16 operands, fp32 accumulator
+ * fragment, element-wise max(x, 0) epilogue, lowering to fp16 on the store)
+ * and by "在 TileLang 中編寫高效能核心：從 GEMM 到 MLA" (section "編寫一個
+ * GEMM": C = ReLU(A @ B) with the ReLU fused before the write-back).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers A, B, C and `workspace` are DEVICE pointers on the current CUDA
+ *    device; the caller allocates and owns them.  The library allocates no
+ *    memory per call.  Per device it keeps a few bytes of state (a status
+ *    word) in a static device variable.
+ *  - Pointers must be at least 2-byte aligned.  When A, B and C are 16-byte
+ *    aligned and K and N are multiples of 8 (16-byte row pitches), operands
+ *    move by TMA; otherwise by plain predicated loads and stores.  Both give
+ *    the same result.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous on it.  The return code covers argument checks and launch
+ *    errors; a device-side watchdog timeout is reported by gemm_relu_status().
+ *  - M, N, K must lie in [0, 2^31 - 1].  M == 0 or N == 0: nothing is written,
+ *    GEMMRELU_OK.  K == 0: C is filled with +0 (the empty sum, then ReLU).
+ *  - C must not overlap A, B or the workspace (not checked).
+ *  - Errors leave C unspecified.  No entry point aborts the process.
+ */
+#ifndef GEMM_RELU_H
+#define GEMM_RELU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMMRELU_OK = 0,
+    GEMMRELU_ERR_INVALID_ARG = 1,        /* null pointer with non-empty size, negative or too large dims, misaligned pointer */
+    GEMMRELU_ERR_UNSUPPORTED_DEVICE = 2, /* current device is not compute capability 10.3 */
+    GEMMRELU_ERR_WORKSPACE = 3,          /* split_k < 1, or workspace null / smaller than the query */
+    GEMMRELU_ERR_LAUNCH = 4,             /* CUDA reported an error configuring or launching a kernel */
+    GEMMRELU_ERR_TIMEOUT = 5,            /* a bounded device-side wait expired (from gemm_relu_status) */
+    GEMMRELU_ERR_CUDA = 6                /* another CUDA runtime error (e.g. while reading the status) */
+} gemmrelu_status;
+
+/*
+ * gemm_relu_f16 -- C = fp16(max(A . B, 0)).
+ *
+ * One fused kernel: TMA (or predicated loads) into a multistage shared-memory
+ * ring, tcgen05.mma into a TMEM fp32 accumulator, ReLU + fp16 cast in the
+ * epilogue, TMA (or predicated) stores.  Tiles of 128 x 256 outputs, a
+ * persistent grid of at most one CTA per SM, grouped (L2-friendly) tile order.
+ *
+ * Returns GEMMRELU_OK or an error code; asynchronous on `stream`.
+ */
+int gemm_relu_f16(const void *A, const void *B, void *C,
+                  int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * gemm_relu_f16_splitk_workspace_bytes -- bytes of device workspace that
+ * gemm_relu_f16_splitk needs for these sizes (0 if no workspace is needed).
+ * Host-only; never touches the device.  Returns 0 for invalid arguments.
+ */
+size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k);
+
+/*
+ * gemm_relu_f16_splitk -- the same C = fp16(max(A . B, 0)), with the K range
+ * cut into `split_k` contiguous pieces computed by different CTAs.
+ *
+ * Follows the split-K scheme of "TileLang 编程基本知识点" section 5.1 (grid
+ * axis over K pieces, each piece offsets only K), taking that page's advice
+ * for reproducibility: instead of fp32 atomic adds into C, every piece writes
+ * its raw fp32 partial to `workspace`, and the last piece to finish a tile
+ * (found with a per-tile arrival counter in the workspace) sums the partials
+ * in the fixed order 0..split_k-1, applies ReLU and writes fp16 C.  Results
+ * are therefore bit-identical from run to run.  ReLU is never applied to a
+ * partial sum.
+ *
+ * The product is computed as C^T = B^T . A^T so that small M maps onto the
+ * narrow (N) side of the MMA; this suits skinny, memory-bound shapes.
+ *
+ * split_k  : >= 1.  Values above ceil(K / 64) are clamped to it.
+ * workspace: device buffer of at least
+ *            gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes,
+ *            16-byte aligned.  Its contents need no initialisation; calls that
+ *            may run concurrently on the GPU must use distinct workspaces.
+ * Needs A, B 16-byte aligned with K and N multiples of 8 (TMA operands);
+ * otherwise, or when split_k == 1, the call runs gemm_relu_f16's kernel and
+ * leaves the workspace untouched.
+ */
+int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
+                         int64_t M, int64_t N, int64_t K, int split_k,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gemm_relu_status -- synchronise `stream`, then return and clear the current
+ * device's watchdog word: GEMMRELU_OK, or GEMMRELU_ERR_TIMEOUT if a bounded
+ * wait inside a kernel expired since the last call (that kernel's output is
+ * then unspecified; the CUDA context stays usable).  Returns GEMMRELU_ERR_CUDA
+ * if the synchronisation or the read fails.
+ */
+int gemm_relu_status(void *stream);
+
+/* gemm_relu_strerror -- static, human-readable text for a status code. */
+const char *gemm_relu_strerror(int code);
+
+/*
+ * gemm_relu_f16_path -- which operand path gemm_relu_f16 would take for these
+ * arguments: 1 = TMA loads and stores, 2 = predicated loads and stores,
+ * 0 = nothing to launch (empty output or K == 0), -1 = invalid arguments.
+ * Host-only; never touches the device.
+ */
+int gemm_relu_f16_path(const void *A, const void *B, const void *C,
+                       int64_t M, int64_t N, int64_t K);
+
+/*
+ * gemm_relu_tile_coord -- the tile rasteriser, evaluated on the host (the
+ * kernels run the same function on the device).  Maps linear tile id `tile`
+ * in [0, m_tiles * n_tiles) to (m_blk, n_blk): tiles are taken in panels of
+ * `panel` consecutive M blocks; inside a panel the id walks down the column
+ * (M fastest) before moving to the next N block -- the grouped launch order
+ * that "在 TileLang 中編寫高效能核心" (section "編寫一個 GEMM",
+ * T.use_swizzle(panel_size=4, order="col")) uses for L2 reuse.
+ * Returns 0, or -1 for out-of-range arguments.
+ */
+int gemm_relu_tile_coord(int64_t tile, int64_t m_tiles, int64_t n_tiles, int panel,
+                         int64_t *m_blk, int64_t *n_blk);
+
+/*
+ * gemm_relu_debug_set -- test hook.  drop_arrive != 0 makes the next launches
+ * skip one producer arrival in CTA 0 (so the consumer's bounded wait expires
+ * and gemm_relu_status reports GEMMRELU_ERR_TIMEOUT); wait_limit_ns sets the
+ * bound of every device-side wait (<= 0 restores the default of one second).
+ * Affects the calling process only.  Returns GEMMRELU_OK.
+ */
+int gemm_relu_debug_set(int drop_arrive, int64_t wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_RELU_H */

@@ -1,0 +1,103 @@
+"""CPU-only: the C-ABI library builds, loads, exports every declared symbol,
+and its host-side logic (argument checks, path choice, rasteriser, workspace
+sizing) behaves as documented.  Nothing here launches a kernel."""
+import os
+import re
+
+import pytest
+
+import tiled_tensor_core_03_gb300 as gr
+from tiled_tensor_core_03_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if _build.needs_build():
+        _build.build()
+    return gr.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("gemm_relu_f16", "gemm_relu_f16_splitk", "gemm_relu_f16_splitk_workspace_bytes",
+                 "gemm_relu_status", "gemm_relu_strerror"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_strerror(lib):
+    for code in range(7):
+        assert gr.strerror(code)
+    assert gr.strerror(999) == "unknown status"
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    c = 0x1000
+    assert gr.gemm_relu_f16(c, c, c, -1, 4, 4) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_f16(c, c, c, 4, 4, 1 << 31) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_f16(c, c, None, 4, 4, 4) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_f16(None, c, c, 4, 4, 4) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_f16(c + 1, c, c, 4, 4, 4) == gr.ERR_INVALID_ARG   # odd address
+    assert gr.gemm_relu_f16_splitk(c, c, c, 4, 4, 4, 0, c, 1 << 20) == gr.ERR_WORKSPACE
+    # empty outputs need no device and no pointers
+    assert gr.gemm_relu_f16(None, None, None, 0, 5, 5) == gr.OK
+    assert gr.gemm_relu_f16(None, None, None, 5, 0, 5) == gr.OK
+
+
+def test_path_choice(lib):
+    a = 0x10000
+    assert gr.gemm_relu_f16_path(a, a, a, 128, 256, 64) == gr.PATH_TMA
+    assert gr.gemm_relu_f16_path(a, a, a, 1537, 1023, 777) == gr.PATH_LSU   # pitches not 16 B
+    assert gr.gemm_relu_f16_path(a + 8, a, a, 128, 256, 64) == gr.PATH_LSU  # A not 16-B aligned
+    assert gr.gemm_relu_f16_path(a, a, a, 128, 256, 60) == gr.PATH_LSU      # K*2 % 16 != 0
+    assert gr.gemm_relu_f16_path(a, a, a, 128, 250, 64) == gr.PATH_LSU
+    assert gr.gemm_relu_f16_path(a, a, a, 0, 256, 64) == gr.PATH_NONE
+    assert gr.gemm_relu_f16_path(a, a, a, 8, 8, 0) == gr.PATH_NONE
+    assert gr.gemm_relu_f16_path(a, a, a, -8, 8, 8) == -1
+
+
+@pytest.mark.parametrize("m_tiles,n_tiles,panel", [(32, 16, 8), (13, 4, 8), (1, 1, 8), (7, 3, 4),
+                                                   (9, 5, 1), (3, 11, 16), (33, 2, 4)])
+def test_rasteriser_is_a_bijection(lib, m_tiles, n_tiles, panel):
+    seen = set()
+    for t in range(m_tiles * n_tiles):
+        mb, nb = gr.gemm_relu_tile_coord(t, m_tiles, n_tiles, panel)
+        assert 0 <= mb < m_tiles and 0 <= nb < n_tiles
+        seen.add((mb, nb))
+    assert len(seen) == m_tiles * n_tiles
+    with pytest.raises(ValueError):
+        gr.gemm_relu_tile_coord(m_tiles * n_tiles, m_tiles, n_tiles, panel)
+
+
+def test_rasteriser_panel_order(lib):
+    # panel 4, column order: ids 0..3 walk down M in N block 0, 4..7 in N block 1
+    coords = [gr.gemm_relu_tile_coord(t, 8, 3, 4) for t in range(12)]
+    assert coords[:5] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1)]
+    assert coords[11] == (3, 2)
+    assert gr.gemm_relu_tile_coord(12, 8, 3, 4) == (4, 0)      # second panel
+
+
+def test_splitk_workspace_size(lib):
+    # 16 x 8192 x 8192, split 8: tickets (64 tiles x 8 B, rounded to 256 B) + 8 x 16 x 8192 fp32
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 8) == 512 + 8 * 16 * 8192 * 4
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 1) == 0
+    # split clamped to the number of 64-wide k blocks
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 128, 100, 8) == 256 + 2 * 16 * 128 * 4
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(0, 8, 8, 2) == 0
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(8, 8, 8, 0) == 0

@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path against the CPU oracle, element by element.
+
+Sizes the oracle finishes in seconds are compared in full; the 4096^3 case
+is compared on sampled rows and elements (plus full-size properties).  The
+tolerance is atol = rtol = 1e-2 per element, and every case must also meet
+the scale-aware bound of gpu_common.compare.
+"""
+import numpy as np
+import pytest
+
+import tiled_tensor_core_03_gb300 as gr
+from tiled_tensor_core_03_gb300 import inputs
+
+from gpu_common import abs_dot, assert_parity, dev, host, run_fused, run_split
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gr.gemm_relu_debug_set(0, 0)
+    yield
+    assert gr.status() == gr.OK
+
+
+# ----------------------------------------------------------------- workloads
+
+
+@pytest.mark.parametrize("name", ["square256", "square1024", "ragged"])
+def test_workload_full(orc, name):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.make_workload(w)
+    want = orc.gemm_relu_f16(A, B)
+    got = run_fused(A, B)
+    assert_parity(got, want, abs_dot(A, B), w.K, name)
+    assert gr.status() == gr.OK
+
+
+def test_ragged_takes_lsu_path_and_aligned_takes_tma():
+    import torch
+    w = inputs.WORKLOADS["ragged"]
+    a = torch.empty((w.M, w.K), dtype=torch.float16, device="cuda")
+    b = torch.empty((w.K, w.N), dtype=torch.float16, device="cuda")
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    assert gr.gemm_relu_f16_path(a.data_ptr(), b.data_ptr(), c.data_ptr(), w.M, w.N, w.K) == gr.PATH_LSU
+    a = torch.empty((1024, 1024), dtype=torch.float16, device="cuda")
+    assert gr.gemm_relu_f16_path(a.data_ptr(), a.data_ptr(), a.data_ptr(), 1024, 1024, 1024) == gr.PATH_TMA
+
+
+def test_square4096_sampled(orc):
+    import torch
+    w = inputs.WORKLOADS["square4096"]
+    A, B = inputs.make_workload(w)
+    a, b = dev(A), dev(B)
+    c = gr.gemm_relu(a, b)
+    got = host(c)
+    # full-size properties
+    assert np.isfinite(got.astype(np.float32)).all()
+    assert (got.astype(np.float32) >= 0).all()
+    # cross-check against cuBLAS fp32 over the whole output (test-only)
+    ref32 = torch.relu(a.float() @ b.float())
+    torch.testing.assert_close(c.float(), ref32, rtol=1e-2, atol=1e-2)
+    # oracle on rows spanning every 128-row block (first and last row of each)
+    rows = sorted({r for mb in range(w.M // 128) for r in (mb * 128, mb * 128 + 127)} | {1, 4095})
+    for r0 in range(0, len(rows), 16):
+        rr = rows[r0:r0 + 16]
+        want = np.concatenate([orc.gemm_relu_f16_rows(A, B, r, 1) for r in rr])
+        assert_parity(got[rr], want, abs_dot(A[rr], B), w.K, f"rows {rr[0]}..")
+    # and random elements everywhere
+    rng = np.random.default_rng(99)
+    I = rng.integers(0, w.M, 4096)
+    J = rng.integers(0, w.N, 4096)
+    want = orc.gemm_relu_f16_at(A, B, I, J)
+    assert_parity(got[I, J], want, abs_dot(A, B, I, J), w.K, "samples")
+
+
+def test_skinny_splitk_full(orc):
+    w = inputs.WORKLOADS["skinny"]
+    A, B = inputs.make_workload(w)
+    want = orc.gemm_relu_f16(A, B)
+    absab = abs_dot(A, B)
+    got = run_split(A, B, w.split_k)
+    assert_parity(got, want, absab, w.K, "skinny split-K")
+    fused = run_fused(A, B)
+    assert_parity(fused, want, absab, w.K, "skinny fused")
+
+
+# ----------------------------------------------------------------- sweeps
+
+TMA_SHAPES = [(m, n, k) for m in (1, 7, 128, 129, 257) for n in (8, 136, 256, 264, 520)
+              for k in (8, 64, 72, 136)]
+LSU_SHAPES = [(m, n, k) for m in (1, 15, 129) for n in (1, 7, 63, 257, 300)
+              for k in (1, 15, 65, 127)]
+
+
+def _sweep(orc, shapes, expect_path):
+    import torch
+    rng = np.random.default_rng(5)
+    bad = []
+    for (M, N, K) in shapes:
+        A = rng.standard_normal((M, K)).astype(np.float16)
+        B = rng.standard_normal((K, N)).astype(np.float16)
+        a, b = dev(A), dev(B)
+        c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        assert gr.gemm_relu_f16_path(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K) == expect_path
+        gr.gemm_relu(a, b, out=c)
+        try:
+            assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, (M, N, K))
+        except AssertionError as e:
+            bad.append(str(e)[:300])
+    assert not bad, bad[:5]
+    assert gr.status() == gr.OK
+
+
+def test_sweep_tma_path(orc):
+    _sweep(orc, TMA_SHAPES, gr.PATH_TMA)
+
+
+def test_sweep_lsu_path(orc):
+    _sweep(orc, LSU_SHAPES, gr.PATH_LSU)
+
+
+SPLIT_CASES = [(1, 128, 64, 2), (16, 120, 1000, 3), (17, 1000, 1000, 3), (33, 256, 4096, 8),
+               (64, 512, 2048, 5), (100, 384, 640, 16), (200, 136, 512, 4), (16, 8, 8192, 8),
+               (130, 264, 256, 2)]
+
+
+@pytest.mark.parametrize("M,N,K,S", SPLIT_CASES)
+def test_splitk_sweep(orc, M, N, K, S):
+    rng = np.random.default_rng(M * 7 + N + K + S)
+    A = rng.standard_normal((M, K)).astype(np.float16)
+    B = rng.standard_normal((K, N)).astype(np.float16)
+    got = run_split(A, B, S)
+    assert_parity(got, orc.gemm_relu_f16(A, B), abs_dot(A, B), K, (M, N, K, S))
+    assert gr.status() == gr.OK
+
+
+def test_splitk_deterministic_and_workspace_contents_irrelevant():
+    import torch
+    w = inputs.WORKLOADS["skinny"]
+    A, B = inputs.make_workload(w)
+    a, b = dev(A), dev(B)
+    ws = gr.splitk_workspace(w.M, w.N, w.K, w.split_k)
+    c1 = gr.gemm_relu_splitk(a, b, w.split_k, workspace=ws).clone()
+    ws.random_(0, 256)                          # garbage, including the counters
+    c2 = gr.gemm_relu_splitk(a, b, w.split_k, workspace=ws).clone()
+    c3 = gr.gemm_relu_splitk(a, b, w.split_k, workspace=ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    assert torch.equal(c1.view(torch.int16), c3.view(torch.int16))
+
+
+# ----------------------------------------------------------------- exact cases
+
+
+@pytest.mark.parametrize("M,N,K", [(1537, 1023, 63), (300, 520, 64), (129, 257, 17), (256, 256, 64)])
+def test_integer_inputs_bit_exact(orc, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-4, 5, (M, K)).astype(np.float16)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float16)
+    got = run_fused(A, B).astype(np.float64)
+    want = orc.gemm_relu_f16(A, B).astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("n", [200, 256])
+def test_identity_gives_relu_of_A(n):
+    rng = np.random.default_rng(n)
+    A = (rng.standard_normal((n, n)) * 3).astype(np.float16)
+    eye = np.eye(n, dtype=np.float16)
+    assert np.array_equal(run_fused(A, eye).astype(np.float64), np.maximum(A, 0).astype(np.float64))
+    assert np.array_equal(run_fused(eye, A).astype(np.float64), np.maximum(A, 0).astype(np.float64))
+
+
+def test_ones_zeros_and_negatives():
+    for (M, N, K) in [(256, 256, 2048), (131, 70, 300)]:
+        ones_a = np.ones((M, K), np.float16)
+        ones_b = np.ones((K, N), np.float16)
+        assert (run_fused(ones_a, ones_b).astype(np.float64) == K).all()
+        assert (run_fused(-ones_a, ones_b).astype(np.float64) == 0).all()
+        assert (run_fused(ones_a, np.zeros((K, N), np.float16)).astype(np.float64) == 0).all()
+
+
+def test_empty_and_k_zero():
+    import torch
+    c = torch.full((4, 5), 7.0, dtype=torch.float16, device="cuda")
+    assert gr.gemm_relu_f16(0, 0, c.data_ptr(), 0, 5, 3, torch.cuda.current_stream().cuda_stream) == gr.OK
+    a = torch.empty((4, 0), dtype=torch.float16, device="cuda")
+    b = torch.empty((0, 5), dtype=torch.float16, device="cuda")
+    out = gr.gemm_relu(a, b, out=c)
+    assert (host(out) == 0).all()
+    c.fill_(7.0)
+    out = gr.gemm_relu_splitk(a, b, 4, out=c)
+    assert (host(out) == 0).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(1537, 1023, 777), (129, 264, 72), (17, 1000, 1000)])
+def test_output_guard_band_untouched(M, N, K):
+    import torch
+    rng = np.random.default_rng(1)
+    A = rng.standard_normal((M, K)).astype(np.float16)
+    B = rng.standard_normal((K, N)).astype(np.float16)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), float("nan"), dtype=torch.float16, device="cuda")
+    c = buf[pad:pad + M * N].view(M, N)
+    gr.gemm_relu(dev(A), dev(B), out=c)
+    if K % 8 == 0 and N % 8 == 0:
+        gr.gemm_relu_splitk(dev(A), dev(B), 3, out=c)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
+    assert not torch.isnan(c).any()
+
+
+def test_error_growth_is_smooth(orc):
+    """The rounding-versus-indexing criterion of the TileLang tutorial's
+    numerics section: error against a wider reference that grows smoothly with
+    the reduction length is rounding; a jump means a dropped or repeated tile.
+    The mean error over positive outputs, relative to the output scale
+    sqrt(K), must stay within a small band of its median over K."""
+    rng = np.random.default_rng(3)
+    rels = []
+    for K in (64, 128, 256, 512, 1024, 2048, 4096, 8192):
+        A = rng.standard_normal((128, K)).astype(np.float16)
+        B = rng.standard_normal((K, 256)).astype(np.float16)
+        g = run_fused(A, B).astype(np.float64)
+        o = orc.gemm_relu_f16(A, B).astype(np.float64)
+        pos = o > 0
+        rels.append(float(np.abs(g - o)[pos].mean() / np.sqrt(K)))
+    med = float(np.median(rels))
+    assert max(rels) <= 4 * med and max(rels) < 1e-3, rels

@@ -1,0 +1,42 @@
+"""GPU watchdog: a dropped producer arrival makes a bounded wait expire; the
+call reports GEMMRELU_ERR_TIMEOUT through gemm_relu_status and the context
+stays usable.  No fault, trap or hang: the wait gives up after 20 ms."""
+import numpy as np
+import pytest
+
+import tiled_tensor_core_03_gb300 as gr
+from tiled_tensor_core_03_gb300 import inputs
+
+from gpu_common import abs_dot, assert_parity, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _restore():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gr.status()
+    yield
+    gr.gemm_relu_debug_set(0, 0)
+    gr.status()
+
+
+@pytest.mark.parametrize("kind", ["tma", "lsu", "splitk"])
+def test_dropped_arrival_times_out_and_recovers(orc, kind):
+    shapes = {"tma": (256, 512, 256), "lsu": (255, 509, 250), "splitk": (16, 1024, 2048)}
+    M, N, K = shapes[kind]
+    A, B = inputs.make(M, N, K, seed=8)
+    a, b = dev(A), dev(B)
+    gr.gemm_relu_debug_set(1, 20_000_000)
+    if kind == "splitk":
+        gr.gemm_relu_splitk(a, b, 4)
+    else:
+        gr.gemm_relu(a, b)
+    assert gr.status() == gr.ERR_TIMEOUT
+    assert gr.status() == gr.OK            # reading clears the word
+    gr.gemm_relu_debug_set(0, 0)
+    c = gr.gemm_relu_splitk(a, b, 4) if kind == "splitk" else gr.gemm_relu(a, b)
+    assert gr.status() == gr.OK
+    assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, kind)

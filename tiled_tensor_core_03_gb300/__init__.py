@@ -1,0 +1,182 @@
+"""Fused fp16 GEMM + ReLU for GB300 (sm_103a): Python binding of libgemmrelu.so.
+
+    C = fp16(max(A @ B, 0)),  A: M x K, B: K x N, row-major fp16, fp32 accumulate.
+
+The functions named like the C entry points (gemm_relu_f16, ...) take raw
+device pointers and sizes exactly as the C ABI in include/gemm_relu.h does;
+`gemm_relu` and `gemm_relu_splitk` accept torch tensors and only marshal
+arguments (PyTorch supplies device memory and streams).  Every arithmetic
+step runs in the library's CUDA kernels; if the library is missing this
+module raises instead of computing anything another way.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgemmrelu.so")
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED_DEVICE = 2
+ERR_WORKSPACE = 3
+ERR_LAUNCH = 4
+ERR_TIMEOUT = 5
+ERR_CUDA = 6
+
+PATH_NONE, PATH_TMA, PATH_LSU = 0, 1, 2
+
+_lib = None
+
+
+class GemmReluError(RuntimeError):
+    def __init__(self, code, what=""):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (status {code})" if what else strerror(code))
+
+
+def lib():
+    """Load libgemmrelu.so (built by __graft_entry__.build() or _build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        L.gemm_relu_f16.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        L.gemm_relu_f16.restype = i32
+        L.gemm_relu_f16_splitk_workspace_bytes.argtypes = [i64, i64, i64, i32]
+        L.gemm_relu_f16_splitk_workspace_bytes.restype = sz
+        L.gemm_relu_f16_splitk.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
+        L.gemm_relu_f16_splitk.restype = i32
+        L.gemm_relu_status.argtypes = [vp]
+        L.gemm_relu_status.restype = i32
+        L.gemm_relu_strerror.argtypes = [i32]
+        L.gemm_relu_strerror.restype = ctypes.c_char_p
+        L.gemm_relu_f16_path.argtypes = [vp, vp, vp, i64, i64, i64]
+        L.gemm_relu_f16_path.restype = i32
+        L.gemm_relu_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
+                                           ctypes.POINTER(i64)]
+        L.gemm_relu_tile_coord.restype = i32
+        L.gemm_relu_debug_set.argtypes = [i32, i64]
+        L.gemm_relu_debug_set.restype = i32
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ C-ABI names
+
+
+def gemm_relu_f16(A, B, C, M, N, K, stream=None):
+    return lib().gemm_relu_f16(A, B, C, M, N, K, stream)
+
+
+def gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k):
+    return lib().gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k)
+
+
+def gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, workspace, workspace_bytes, stream=None):
+    return lib().gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, workspace, workspace_bytes,
+                                      stream)
+
+
+def gemm_relu_status(stream=None):
+    return lib().gemm_relu_status(stream)
+
+
+def gemm_relu_strerror(code):
+    return lib().gemm_relu_strerror(code).decode()
+
+
+strerror = gemm_relu_strerror
+
+
+def gemm_relu_f16_path(A, B, C, M, N, K):
+    return lib().gemm_relu_f16_path(A, B, C, M, N, K)
+
+
+def gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel):
+    mb, nb = ctypes.c_int64(), ctypes.c_int64()
+    rc = lib().gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel, ctypes.byref(mb),
+                                    ctypes.byref(nb))
+    if rc != 0:
+        raise ValueError("tile out of range")
+    return mb.value, nb.value
+
+
+def gemm_relu_debug_set(drop_arrive=0, wait_limit_ns=0):
+    return lib().gemm_relu_debug_set(int(drop_arrive), int(wait_limit_ns))
+
+
+# ------------------------------------------------------------------ torch helpers
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_operands(a, b):
+    import torch
+    if a.dtype != torch.float16 or b.dtype != torch.float16:
+        raise TypeError("A and B must be torch.float16")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"shapes {tuple(a.shape)} and {tuple(b.shape)} do not multiply")
+    if not (a.is_cuda and b.is_cuda and a.device == b.device):
+        raise ValueError("A and B must be CUDA tensors on the same device")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("A and B must be contiguous row-major")
+
+
+def _out(a, b, out):
+    import torch
+    M, N = a.shape[0], b.shape[1]
+    if out is None:
+        return torch.empty((M, N), dtype=torch.float16, device=a.device)
+    if out.shape != (M, N) or out.dtype != torch.float16 or not out.is_contiguous() \
+            or out.device != a.device:
+        raise ValueError("out must be a contiguous float16 (M, N) tensor on A's device")
+    return out
+
+
+def gemm_relu(a, b, out=None, stream=None):
+    """C = relu(a @ b) in fp16 with fp32 accumulation (one fused kernel)."""
+    _check_operands(a, b)
+    c = _out(a, b, out)
+    M, K = a.shape
+    N = b.shape[1]
+    rc = gemm_relu_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, _stream_ptr(stream))
+    if rc != OK:
+        raise GemmReluError(rc, "gemm_relu_f16")
+    return c
+
+
+def splitk_workspace(M, N, K, split_k, device=None):
+    """A device workspace sized for gemm_relu_splitk (uint8 tensor, may be empty)."""
+    import torch
+    n = gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def gemm_relu_splitk(a, b, split_k, out=None, workspace=None, stream=None):
+    """Same result as gemm_relu, with K split into `split_k` pieces and a
+    deterministic in-kernel reduction (for skinny, memory-bound shapes)."""
+    _check_operands(a, b)
+    c = _out(a, b, out)
+    M, K = a.shape
+    N = b.shape[1]
+    if workspace is None:
+        workspace = splitk_workspace(M, N, K, split_k, a.device)
+    rc = gemm_relu_f16_splitk(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, split_k,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                              _stream_ptr(stream))
+    if rc != OK:
+        raise GemmReluError(rc, "gemm_relu_f16_splitk")
+    return c
+
+
+def status(stream=None):
+    """Synchronise and return (and clear) the device watchdog status."""
+    return gemm_relu_status(_stream_ptr(stream))

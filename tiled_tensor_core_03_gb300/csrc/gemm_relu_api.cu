@@ -1,0 +1,373 @@
+// gemm_relu_api.cu -- the C ABI of libgemmrelu.so (declared in gemm_relu.h).
+//
+// Host side only: argument checks, choice of operand path, TMA tensor-map
+// encoding (CUDA driver entry point fetched through the runtime, so the
+// library needs no link against libcuda), launch configuration and the
+// device status word.  Every arithmetic step runs in the kernels of
+// gemm_relu_kernels.cuh; there is no host or library fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_relu.h"
+#include "gemm_relu_kernels.cuh"
+
+namespace {
+
+using gemmrelu::tile_coord;
+
+constexpr int64_t kMaxDim = 0x7fffffff;
+constexpr int kPanel = 8;                       // M blocks per rasteriser panel
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;
+
+// ---------------------------------------------------------------- test hooks
+std::atomic<int> g_drop_arrive{0};
+std::atomic<int64_t> g_wait_limit_ns{0};
+std::atomic<uint32_t> g_epoch{0};
+
+uint64_t wait_limit_ns() {
+    const int64_t v = g_wait_limit_ns.load();
+    return v > 0 ? (uint64_t)v : kDefaultWaitLimitNs;
+}
+
+// ---------------------------------------------------------------- per device
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    bool attr_fused[2] = {false, false};
+    bool attr_split[4] = {false, false, false, false};
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int current_device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return GEMMRELU_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &s = g_dev[dev];
+    if (!s.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMMRELU_ERR_CUDA;
+        s.supported = (major == 10 && minor == 3);
+        s.sms = sms;
+        s.probed = true;
+    }
+    *out = &s;
+    return s.supported ? GEMMRELU_OK : GEMMRELU_ERR_UNSUPPORTED_DEVICE;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major fp16 matrix rows x cols (cols contiguous), box box_cols x box_rows,
+// 128-byte swizzle, zero fill outside the matrix.
+bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
+              uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- argument checks
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_args(const void *A, const void *B, const void *C, int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMMRELU_ERR_INVALID_ARG;
+    if (M == 0 || N == 0)
+        return GEMMRELU_OK;
+    if (!C || !aligned(C, 2))
+        return GEMMRELU_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B || !aligned(A, 2) || !aligned(B, 2)))
+        return GEMMRELU_ERR_INVALID_ARG;
+    return GEMMRELU_OK;
+}
+
+// TMA can describe a row-major fp16 matrix when its base is 16-byte aligned
+// and its row pitch (cols * 2 bytes) is a multiple of 16 bytes.
+bool tma_ok(const void *p, int64_t cols) { return aligned(p, 16) && (cols % 8) == 0; }
+
+int fused_path(const void *A, const void *B, const void *C, int64_t M, int64_t N, int64_t K) {
+    if (check_args(A, B, C, M, N, K) != GEMMRELU_OK)
+        return -1;
+    if (M == 0 || N == 0 || K == 0)
+        return 0;
+    return (tma_ok(A, K) && tma_ok(B, N) && tma_ok(C, N)) ? 1 : 2;
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? GEMMRELU_OK : GEMMRELU_ERR_LAUNCH; }
+
+template <typename Kern>
+bool ensure_smem_attr(bool &done, Kern kernel, uint32_t bytes) {
+    if (done)
+        return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return false;
+    done = true;
+    return true;
+}
+
+int zero_fill(void *C, int64_t M, int64_t N, cudaStream_t stream) {
+    return launch_status(cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * 2, stream));
+}
+
+// ---------------------------------------------------------------- fused launch
+int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                 cudaStream_t stream, DeviceState *ds) {
+    namespace F = gemmrelu::fused;
+    const int path = fused_path(A, B, C, M, N, K);
+    F::Params p{};
+    p.A = static_cast<const uint16_t *>(A);
+    p.B = static_cast<const uint16_t *>(B);
+    p.C = static_cast<uint16_t *>(C);
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.num_kb = (int)((K + F::BK - 1) / F::BK);
+    p.m_tiles = (M + F::BM - 1) / F::BM;
+    p.n_tiles = (N + F::BN - 1) / F::BN;
+    p.num_tiles = p.m_tiles * p.n_tiles;
+    p.panel = kPanel;
+    p.drop_arrive = g_drop_arrive.load();
+    p.wait_limit_ns = wait_limit_ns();
+    const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
+
+    CUtensorMap mA, mB, mC;
+    std::memset(&mA, 0, sizeof(mA));
+    std::memset(&mB, 0, sizeof(mB));
+    std::memset(&mC, 0, sizeof(mC));
+    if (path == 1) {
+        if (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
+            !make_map(&mC, C, M, N, 64, 32))
+            return GEMMRELU_ERR_LAUNCH;
+        auto kern = F::gemm_relu_fused_kernel<true>;
+        if (!ensure_smem_attr(ds->attr_fused[0], kern, F::kSmemBytes))
+            return GEMMRELU_ERR_LAUNCH;
+        kern<<<(unsigned)grid, F::Roles<true>::kThreads, F::kSmemBytes, stream>>>(mA, mB, mC, p);
+    } else {
+        auto kern = F::gemm_relu_fused_kernel<false>;
+        if (!ensure_smem_attr(ds->attr_fused[1], kern, F::kSmemBytes))
+            return GEMMRELU_ERR_LAUNCH;
+        kern<<<(unsigned)grid, F::Roles<false>::kThreads, F::kSmemBytes, stream>>>(mA, mB, mC, p);
+    }
+    return launch_status(cudaGetLastError());
+}
+
+// ---------------------------------------------------------------- split-K
+namespace S = gemmrelu::splitk;
+
+int split_bms(int64_t M) {
+    if (M <= 16)
+        return 16;
+    if (M <= 32)
+        return 32;
+    if (M <= 64)
+        return 64;
+    return 128;
+}
+
+int effective_splits(int64_t K, int split_k) {
+    const int64_t num_kb = (K + S::BK - 1) / S::BK;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(split_k, num_kb));
+}
+
+struct SplitLayout {
+    int bms, splits;
+    int64_t n_tiles, m_tiles, tickets_bytes, part_bytes;
+};
+
+SplitLayout split_layout(int64_t M, int64_t N, int64_t K, int split_k) {
+    SplitLayout L{};
+    L.bms = split_bms(M);
+    L.splits = effective_splits(K, split_k);
+    L.n_tiles = (N + S::BNT - 1) / S::BNT;
+    L.m_tiles = (M + L.bms - 1) / L.bms;
+    L.tickets_bytes = ((L.n_tiles * L.m_tiles * 8 + 255) / 256) * 256;
+    L.part_bytes = (int64_t)L.splits * M * N * 4;
+    return L;
+}
+
+template <int BMS>
+int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                     const SplitLayout &L, void *ws, cudaStream_t stream, DeviceState *ds,
+                     bool &attr_done) {
+    using G = S::Cfg<BMS>;
+    S::Params p{};
+    p.C = static_cast<uint16_t *>(C);
+    p.tickets = static_cast<unsigned long long *>(ws);
+    p.part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.tickets_bytes);
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.num_kb = (int)((K + S::BK - 1) / S::BK);
+    p.splits = L.splits;
+    p.n_tiles = L.n_tiles;
+    p.m_tiles = L.m_tiles;
+    p.num_units = L.n_tiles * L.m_tiles * L.splits;
+    uint32_t e = ++g_epoch;
+    if (e == 0)
+        e = ++g_epoch;
+    p.epoch = e;
+    p.drop_arrive = g_drop_arrive.load();
+    p.wait_limit_ns = wait_limit_ns();
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, M, K, S::BK, BMS) || !make_map(&mB, B, K, N, 64, S::BK))
+        return GEMMRELU_ERR_LAUNCH;
+    auto kern = S::gemm_relu_splitk_kernel<BMS>;
+    if (!ensure_smem_attr(attr_done, kern, G::kSmemBytes))
+        return GEMMRELU_ERR_LAUNCH;
+    const int64_t grid = std::min<int64_t>(p.num_units, ds->sms);
+    kern<<<(unsigned)grid, 192, G::kSmemBytes, stream>>>(mA, mB, p);
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+extern "C" {
+
+int gemm_relu_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                  void *stream) {
+    int rc = check_args(A, B, C, M, N, K);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return GEMMRELU_OK;
+    DeviceState *ds = nullptr;
+    rc = current_device_state(&ds);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return zero_fill(C, M, N, s);
+    return launch_fused(A, B, C, M, N, K, s, ds);
+}
+
+size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || split_k < 1)
+        return 0;
+    const SplitLayout L = split_layout(M, N, K, split_k);
+    if (L.splits <= 1)
+        return 0;
+    return (size_t)(L.tickets_bytes + L.part_bytes);
+}
+
+int gemm_relu_f16_splitk(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                         int split_k, void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_args(A, B, C, M, N, K);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    if (split_k < 1)
+        return GEMMRELU_ERR_WORKSPACE;
+    if (M == 0 || N == 0)
+        return GEMMRELU_OK;
+    DeviceState *ds = nullptr;
+    rc = current_device_state(&ds);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return zero_fill(C, M, N, s);
+    const SplitLayout L = split_layout(M, N, K, split_k);
+    if (L.splits <= 1 || !tma_ok(A, K) || !tma_ok(B, N))
+        return launch_fused(A, B, C, M, N, K, s, ds);
+    const size_t need = (size_t)(L.tickets_bytes + L.part_bytes);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+        return GEMMRELU_ERR_WORKSPACE;
+    switch (L.bms) {
+    case 16:
+        return launch_split_bms<16>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[0]);
+    case 32:
+        return launch_split_bms<32>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[1]);
+    case 64:
+        return launch_split_bms<64>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[2]);
+    default:
+        return launch_split_bms<128>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[3]);
+    }
+}
+
+int gemm_relu_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMMRELU_ERR_CUDA;
+    unsigned int st = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&st, gemmrelu::g_status, sizeof(st)) != cudaSuccess)
+        return GEMMRELU_ERR_CUDA;
+    if (st != 0 && cudaMemcpyToSymbol(gemmrelu::g_status, &zero, sizeof(zero)) != cudaSuccess)
+        return GEMMRELU_ERR_CUDA;
+    return (int)st;
+}
+
+const char *gemm_relu_strerror(int code) {
+    switch (code) {
+    case GEMMRELU_OK: return "ok";
+    case GEMMRELU_ERR_INVALID_ARG: return "invalid argument";
+    case GEMMRELU_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (sm_103a)";
+    case GEMMRELU_ERR_WORKSPACE: return "split_k < 1 or workspace missing, misaligned or too small";
+    case GEMMRELU_ERR_LAUNCH: return "CUDA error configuring or launching a kernel";
+    case GEMMRELU_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case GEMMRELU_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+    }
+}
+
+int gemm_relu_f16_path(const void *A, const void *B, const void *C, int64_t M, int64_t N,
+                       int64_t K) {
+    return fused_path(A, B, C, M, N, K);
+}
+
+int gemm_relu_tile_coord(int64_t tile, int64_t m_tiles, int64_t n_tiles, int panel, int64_t *m_blk,
+                         int64_t *n_blk) {
+    if (!m_blk || !n_blk || m_tiles <= 0 || n_tiles <= 0 || panel <= 0 || tile < 0 ||
+        tile >= m_tiles * n_tiles)
+        return -1;
+    int64_t mb, nb;
+    tile_coord(tile, m_tiles, n_tiles, panel, mb, nb);
+    *m_blk = mb;
+    *n_blk = nb;
+    return 0;
+}
+
+int gemm_relu_debug_set(int drop_arrive, int64_t wait_limit_ns_arg) {
+    g_drop_arrive.store(drop_arrive ? 1 : 0);
+    g_wait_limit_ns.store(wait_limit_ns_arg > 0 ? wait_limit_ns_arg : 0);
+    return GEMMRELU_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,819 @@
+// gemm_relu_kernels.cuh -- device code of the fused fp16 GEMM + ReLU.
+//
+//   C = fp16( max( A . B , 0 ) ),  A: M x K, B: K x N, C: M x N, row-major.
+//
+// The operation is the FP16 GEMM + ReLU quickstart of "TileLang 编程基本知识点"
+// (section 二) and the GEMM section of "在 TileLang 中編寫高效能核心：從 GEMM 到
+// MLA": fp16 tiles staged in shared memory, a K loop over BK-wide strips,
+// tensor-core MMA into an fp32 accumulator, max(x, 0) on the accumulator, one
+// cast to fp16 on the way out.  The pages' A100/H100 lowering (cp.async or
+// TMA, mma.sync or wgmma) is replaced here by the sm_103a path the same
+// page's section 四/5.4 names for datacenter Blackwell -- TMA + mbarrier
+// pipeline, tcgen05.mma with a TMEM accumulator -- written by hand:
+//
+//   warp 0 (or warps 0-3)  producer: TMA (or predicated loads) into a ring of
+//                          kStages shared-memory stages, full/empty mbarriers
+//   next warp              MMA issuer: one thread issues tcgen05.mma into one
+//                          of two TMEM accumulators, commits to mbarriers
+//   last 4 warps           epilogue: tcgen05.ld -> ReLU -> fp16 -> swizzled
+//                          shared staging -> TMA store (or predicated stores)
+//
+// Roles iterate the same persistent sequence of output tiles (grid = at most
+// one CTA per SM, "TileLang tutorial", chapter "Persistent kernel"), taken in
+// grouped order for L2 reuse (T.use_swizzle(panel_size, order="col") on the
+// atlascloud page).  Every mbarrier wait is bounded by wall-clock time; on
+// expiry the CTA records GEMMRELU_ERR_TIMEOUT in a device status word, every
+// role leaves its loop, in-flight copies are drained and TMEM is freed.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "sm103.cuh"
+
+namespace gemmrelu {
+
+using namespace sm103;
+
+// ------------------------------------------------------------------ status
+
+// Device watchdog word: 0, or the first error code recorded since the host
+// last read it.  `g_status_where` tells which wait expired (debugging aid).
+__device__ unsigned int g_status;
+__device__ unsigned int g_status_where;
+
+constexpr unsigned kStatusTimeout = 5;  // == GEMMRELU_ERR_TIMEOUT
+
+enum WaitSite : unsigned {
+    kSiteProducerEmpty = 1,
+    kSiteMmaAccEmpty = 2,
+    kSiteMmaFull = 3,
+    kSiteEpiAccFull = 4,
+    kSiteDrain = 5,
+    kSiteTicket = 6,
+};
+
+__device__ __forceinline__ void record_timeout(volatile uint32_t *abort_flag, unsigned where) {
+    *abort_flag = 1u;
+    if (atomicCAS(&g_status, 0u, kStatusTimeout) == 0u)
+        g_status_where = where;
+}
+
+// Wait for the phase of parity `parity` of mbarrier `bar`; give up after
+// `limit_ns` of wall-clock time (recording a timeout) or as soon as another
+// role of this CTA has given up.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile uint32_t *abort_flag, unsigned where) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout(abort_flag, where);
+            return false;
+        }
+    }
+}
+
+// Same, but ignores the abort flag: used to drain work already in flight.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                           volatile uint32_t *abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout(abort_flag, kSiteDrain);
+            return false;
+        }
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ rasteriser
+
+// Linear tile id -> (m block, n block).  Panels of `panel` consecutive M
+// blocks; inside a panel M varies fastest, then N; panels follow in M order.
+// The last panel may hold fewer M blocks.  A bijection on [0, m_tiles*n_tiles).
+__host__ __device__ __forceinline__ void tile_coord(int64_t t, int64_t m_tiles, int64_t n_tiles,
+                                                    int64_t panel, int64_t &mb, int64_t &nb) {
+    const int64_t per_panel = panel * n_tiles;
+    const int64_t p = t / per_panel;
+    const int64_t r = t - p * per_panel;
+    const int64_t left = m_tiles - p * panel;
+    const int64_t rows = left < panel ? left : panel;
+    mb = p * panel + r % rows;
+    nb = r / rows;
+}
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ uint32_t relu_pack_half2(uint32_t lo_bits, uint32_t hi_bits) {
+    const float lo = fmaxf(__uint_as_float(lo_bits), 0.0f);
+    const float hi = fmaxf(__uint_as_float(hi_bits), 0.0f);
+    const __half2 h = __floats2half2_rn(lo, hi);  // .x (low half) = lo
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Byte offset of 16-byte chunk j of row r inside a 128-byte-swizzled tile
+// whose rows are 128 bytes: the chunk index is XORed with (row mod 8), the
+// pattern TMA's SWIZZLE_128B mode writes and tcgen05's SWIZZLE_128B reads.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t j) {
+    return r * 128u + ((j ^ (r & 7u)) << 4);
+}
+
+// Eight fp16 values src[col0 .. col0+7] of one row (zero where col >= limit),
+// packed in a uint4.  Uses one 16-byte load when aligned and fully inside.
+__device__ __forceinline__ uint4 load8_pred(const uint16_t *__restrict__ row, int64_t col0,
+                                            int64_t limit) {
+    const uint16_t *p = row + col0;
+    if (col0 + 8 <= limit && (reinterpret_cast<uintptr_t>(p) & 15u) == 0)
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = (col0 + 2 * e < limit) ? (uint32_t)__ldg(p + 2 * e) : 0u;
+        const uint32_t hi = (col0 + 2 * e + 1 < limit) ? (uint32_t)__ldg(p + 2 * e + 1) : 0u;
+        w[e] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// tcgen05.ld of 32 / 16 columns fused with its wait, so that no use of the
+// destination registers can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld_x32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+          "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// ================================================================== fused kernel
+
+namespace fused {
+
+constexpr int BM = 128;            // UMMA M: TMEM lanes = output rows
+constexpr int BN = 256;            // UMMA N: TMEM columns per accumulator
+constexpr int BK = 64;             // one 128-byte swizzle row of fp16
+constexpr int UK = 16;             // K of one tcgen05.mma kind::f16
+constexpr int kStages = 4;
+constexpr uint32_t kATile = BM * BK * 2;    // 16 KB, K-major, 128 rows x 128 B
+constexpr uint32_t kBSlab = BK * 64 * 2;    // 8 KB: 64 k-rows x 64 n (128 B)
+constexpr uint32_t kBTile = BK * BN * 2;    // 32 KB = 4 slabs, MN-major
+constexpr uint32_t kEpiBuf = 32 * 128;      // 32 rows x 64 fp16, swizzled
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kTmemCols = 2 * BN;      // double-buffered accumulator
+
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kATile;
+constexpr uint32_t kOffEpi = kOffB + kStages * kBTile;
+constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
+constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+
+// A: K-major (bit 15 = 0); B: N-major (bit 16 = 1); M = 128, N = 256.
+constexpr uint32_t kIdesc = make_idesc_f16_f32(BM, BN, 0, 1);
+
+struct Params {
+    const uint16_t *A;
+    const uint16_t *B;
+    uint16_t *C;
+    int M, N, K;
+    int num_kb;
+    int64_t m_tiles, n_tiles, num_tiles;
+    int panel;
+    int drop_arrive;
+    uint64_t wait_limit_ns;
+};
+
+template <bool kTma>
+struct Roles {
+    static constexpr int kLoadWarps = kTma ? 1 : 4;
+    static constexpr int kMmaWarp = kLoadWarps;
+    static constexpr int kEpiWarp0 = kLoadWarps + 1;
+    static constexpr int kThreads = 32 * (kLoadWarps + 1 + kEpiWarps);
+};
+
+template <bool kTma>
+__global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
+    gemm_relu_fused_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const Params p) {
+    using R = Roles<kTma>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t bar0 = base + kOffBar;
+    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kStages + s); };
+    auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
+    auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffMisc);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), kTma ? 1u : 32u * R::kLoadWarps);
+            mbar_init(empty_bar(s), 1u);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1u);
+            mbar_init(acce_bar(b), (uint32_t)kEpiWarps);
+        }
+        mbar_init(drain_bar, 1u);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (kTma && warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmC);
+    }
+    if (warp == R::kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    if (warp < R::kLoadWarps) {
+        // ============================================================ producer
+        if constexpr (kTma) {
+            if (lane == 0) {
+                uint32_t stage = 0, phase = 0, issued = 0, parity = 0;
+                bool ok = true;
+                for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                    int64_t mb, nb;
+                    tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
+                    const int m0 = (int)(mb * BM), n0 = (int)(nb * BN);
+                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                        if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
+                                          kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        const bool drop =
+                            p.drop_arrive && blockIdx.x == 0 && t == blockIdx.x && kb == 0;
+                        if (!drop) {
+                            const uint32_t fb = full_bar(stage);
+                            mbar_arrive_expect_tx(fb, kATile + kBTile);
+                            tma_load_2d(&tmA, base + kOffA + stage * kATile, fb, kb * BK, m0);
+                            const uint32_t bdst = base + kOffB + stage * kBTile;
+#pragma unroll
+                            for (int j = 0; j < BN / 64; ++j)
+                                tma_load_2d(&tmB, bdst + j * kBSlab, fb, n0 + 64 * j, kb * BK);
+                            issued |= 1u << stage;
+                            parity = (parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                // Every copy issued must have landed before the CTA may exit.
+                for (uint32_t s = 0; s < kStages; ++s)
+                    if (issued & (1u << s))
+                        wait_drain(full_bar(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
+            }
+        } else {
+            // Predicated loads for operands TMA cannot describe (row pitches
+            // that are not multiples of 16 bytes).  Same swizzled layout.
+            const int tid = threadIdx.x;  // 0 .. 127
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int64_t mb, nb;
+                tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
+                const int64_t m0 = mb * BM, n0 = nb * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
+                                      kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t k0 = (int64_t)kb * BK;
+                    const uint32_t adst = base + kOffA + stage * kATile;
+                    for (int c = tid; c < BM * 8; c += 128) {
+                        const int r = c >> 3, j = c & 7;
+                        const int64_t gm = m0 + r;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (gm < p.M)
+                            v = load8_pred(p.A + gm * p.K, k0 + 8 * j, p.K);
+                        st_shared_v4(adst + sw128_offset(r, j), v.x, v.y, v.z, v.w);
+                    }
+                    const uint32_t bdst = base + kOffB + stage * kBTile;
+                    for (int c = tid; c < BK * (BN / 8); c += 128) {
+                        const int j = c & 7, s = (c >> 3) & 3, r = c >> 5;
+                        const int64_t gk = k0 + r;
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (gk < p.K)
+                            v = load8_pred(p.B + gk * p.N, n0 + 64 * s + 8 * j, p.N);
+                        st_shared_v4(bdst + s * kBSlab + sw128_offset(r, j), v.x, v.y, v.z, v.w);
+                    }
+                    fence_proxy_async_smem();
+                    const bool drop =
+                        p.drop_arrive && blockIdx.x == 0 && t == blockIdx.x && kb == 0;
+                    if (!drop)
+                        mbar_arrive(full_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == R::kMmaWarp) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int64_t i = 0;
+            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++i) {
+                const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
+                if (!wait_bounded(acce_bar(buf), use ^ 1u, p.wait_limit_ns, abort_flag,
+                                  kSiteMmaAccEmpty))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + buf * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
+                                      kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a = base + kOffA + stage * kATile;
+                    const uint32_t b = base + kOffB + stage * kBTile;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk) {
+                        // A (K-major): the next 16 k are 32 bytes further
+                        // along each swizzled row; 8-row groups 1024 B apart.
+                        const uint64_t adesc = make_sdesc_sw128(a + kk * (UK * 2), 16, 1024);
+                        // B (N-major): the next 16 k are 16 rows of 128 B
+                        // further; 64-wide N slabs kBSlab apart (LBO), 8-row
+                        // k groups 1024 B apart (SBO).
+                        const uint64_t bdesc = make_sdesc_sw128(b + kk * (UK * 128), kBSlab, 1024);
+                        umma_f16(d, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(accf_bar(buf));
+            }
+            // All MMAs of this thread complete before TMEM can be released.
+            umma_commit(drain_bar);
+            wait_drain(drain_bar, 0u, p.wait_limit_ns, abort_flag);
+        }
+    } else {
+        // ============================================================ epilogue
+        const int ew = warp - R::kEpiWarp0;     // staging buffer owner 0..3
+        const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * 2u * kEpiBuf;
+        uint32_t nstores = 0;
+        int64_t i = 0;
+        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
+            const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
+                                         kSiteEpiAccFull);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after_sync();
+            int64_t mb, nb;
+            tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
+            const int64_t row0 = mb * BM + 32 * q;
+            const int64_t n0 = nb * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 64; ++c) {
+                const int64_t col0 = n0 + 64 * c;
+                if (row0 >= p.M || col0 >= p.N)
+                    continue;  // warp-uniform: nothing of this chunk is in C
+                uint32_t r[32], h[32];
+                const uint32_t taddr = tmem_base + lane_base + buf * BN + 64 * c;
+                tmem_ld_x32_sync(taddr, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
+                tmem_ld_x32_sync(taddr + 32, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
+
+                if constexpr (kTma) {
+                    const uint32_t sb = stage_base + (nstores & 1u) * kEpiBuf;
+                    // the store issued two chunks ago from this buffer must
+                    // have finished reading it
+                    if (lane == 0)
+                        bulk_wait_group_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(sb + sw128_offset(lane, j), h[4 * j], h[4 * j + 1],
+                                     h[4 * j + 2], h[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, sb, (int32_t)col0, (int32_t)row0);
+                        bulk_commit_group();
+                    }
+                    ++nstores;
+                } else {
+                    const uint32_t sb = stage_base;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(sb + sw128_offset(lane, j), h[4 * j], h[4 * j + 1],
+                                     h[4 * j + 2], h[4 * j + 3]);
+                    __syncwarp();
+                    // warp writes row by row: lane l owns columns 2l, 2l+1
+                    const int64_t col = col0 + 2 * lane;
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int64_t row = row0 + rr;
+                        if (row >= p.M)
+                            break;
+                        const uint32_t w = ld_shared_b32(sb + rr * 128u +
+                                                         ((((uint32_t)lane >> 2) ^ (rr & 7u)) << 4) +
+                                                         ((uint32_t)lane & 3u) * 4u);
+                        uint16_t *dst = p.C + row * p.N + col;
+                        if (col < p.N)
+                            dst[0] = (uint16_t)(w & 0xffffu);
+                        if (col + 1 < p.N)
+                            dst[1] = (uint16_t)(w >> 16);
+                    }
+                    __syncwarp();
+                }
+            }
+            // accumulator buffer fully read: hand it back to the MMA warp
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce_bar(buf));
+        }
+        if constexpr (kTma) {
+            if (lane == 0)
+                bulk_wait_group<0>();
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == R::kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace fused
+
+// ================================================================== split-K kernel
+//
+// C^T = B^T . A^T per K piece: the MMA's M side (128 TMEM lanes) runs over N
+// and its narrow N side (BMS columns) over M, so M = 16 costs a 128 x 16 MMA
+// instead of a 128-row tile mostly empty.  UMMA A operand = a B tile,
+// N-major; UMMA B operand = an A tile, K-major.  Each work unit (n tile,
+// m tile, split s) accumulates k blocks [s*kb/S, (s+1)*kb/S) and writes its
+// raw fp32 partial to the workspace; the last unit of a tile to finish (an
+// arrival counter per tile, tagged with the call's epoch) sums the S
+// partials in order 0..S-1, applies ReLU, rounds to fp16 and writes C.
+
+namespace splitk {
+
+constexpr int BNT = 128;                     // N per tile (UMMA M)
+constexpr int BK = 64;
+constexpr int UK = 16;
+constexpr uint32_t kBSlab = BK * 64 * 2;     // 8 KB
+constexpr uint32_t kBTile = BK * BNT * 2;    // 16 KB = 2 slabs
+constexpr int kEpiWarps = 4;
+
+template <int BMS>
+struct Cfg {
+    static constexpr uint32_t kATile = BMS * BK * 2;            // K-major, BMS rows
+    static constexpr uint32_t kStageBytes = kBTile + kATile;
+    static constexpr uint32_t kBudget = 227u * 1024u - 1024u - 256u;
+    static constexpr int kStagesRaw = (int)(kBudget / kStageBytes);
+    static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+    static constexpr uint32_t kOffBar = kStages * kStageBytes;
+    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr uint32_t kTmemCols = (2 * BMS < 32) ? 32 : 2 * BMS;  // power of 2
+    // UMMA A (the B tile) N-major: bit 15 = 1; UMMA B (the A tile) K-major.
+    static constexpr uint32_t kIdesc = make_idesc_f16_f32(BNT, BMS, 1, 0);
+};
+
+struct Params {
+    uint16_t *C;
+    float *part;                       // [S][M][N] fp32
+    unsigned long long *tickets;       // [m_tiles * n_tiles]
+    int M, N, K;
+    int num_kb, splits;
+    int64_t n_tiles, m_tiles, num_units;
+    uint32_t epoch;
+    int drop_arrive;
+    uint64_t wait_limit_ns;
+};
+
+// Per-tile arrival counter: word = (epoch << 32) | count.  A word carrying
+// another epoch (stale, or never used) counts as zero.  The arrival that
+// brings the count to `splits` is the last; it resets the word to 0.
+__device__ __forceinline__ int ticket_arrive(unsigned long long *w, uint32_t epoch,
+                                             uint32_t splits, volatile uint32_t *abort_flag) {
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(w);
+    for (int it = 0; it < (1 << 20); ++it) {
+        const uint32_t e = (uint32_t)(old >> 32);
+        const uint32_t c = (uint32_t)old;
+        const uint32_t nc = (e == epoch) ? c + 1u : 1u;
+        const unsigned long long nw =
+            (nc >= splits) ? 0ull : (((unsigned long long)epoch << 32) | nc);
+        const unsigned long long prev = atomicCAS(w, old, nw);
+        if (prev == old)
+            return nc >= splits ? 1 : 0;
+        old = prev;
+    }
+    record_timeout(abort_flag, kSiteTicket);
+    return -1;
+}
+
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <int BMS>
+__global__ void __launch_bounds__(192, 1)
+    gemm_relu_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+    using G = Cfg<BMS>;
+    constexpr int kStages = G::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t bar0 = base + G::kOffBar;
+    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kStages + s); };
+    auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
+    auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + G::kOffMisc);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 4);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(gbase + G::kOffMisc + 8);
+    volatile uint32_t *decision = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 12);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t S = p.splits;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+            mbar_init(full_bar(s), 1u);
+            mbar_init(empty_bar(s), 1u);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1u);
+            mbar_init(acce_bar(b), (uint32_t)kEpiWarps);
+        }
+        mbar_init(drain_bar, 1u);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), G::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    auto unit_coords = [&](int64_t u, int64_t &s, int64_t &nt, int64_t &mt, int &kb0, int &kb1) {
+        s = u % S;
+        const int64_t tile = u / S;
+        nt = tile % p.n_tiles;
+        mt = tile / p.n_tiles;
+        kb0 = (int)((s * p.num_kb) / S);
+        kb1 = (int)(((s + 1) * p.num_kb) / S);
+    };
+
+    if (warp == 0) {
+        // ============================================================ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, parity = 0, issued = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+                int64_t s, nt, mt;
+                int kb0, kb1;
+                unit_coords(u, s, nt, mt, kb0, kb1);
+                const int n0 = (int)(nt * BNT), m0 = (int)(mt * BMS);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
+                                      kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool drop = p.drop_arrive && blockIdx.x == 0 && u == blockIdx.x && kb == kb0;
+                    if (!drop) {
+                        const uint32_t fb = full_bar(stage);
+                        const uint32_t dst = base + stage * G::kStageBytes;
+                        mbar_arrive_expect_tx(fb, G::kStageBytes);
+                        tma_load_2d(&tmB, dst, fb, n0, kb * BK);
+                        tma_load_2d(&tmB, dst + kBSlab, fb, n0 + 64, kb * BK);
+                        tma_load_2d(&tmA, dst + kBTile, fb, kb * BK, m0);
+                        issued |= 1u << stage;
+                        parity = (parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    if (++stage == (uint32_t)kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            for (uint32_t s = 0; s < (uint32_t)kStages; ++s)
+                if (issued & (1u << s))
+                    wait_drain(full_bar(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int64_t i = 0;
+            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++i) {
+                int64_t s, nt, mt;
+                int kb0, kb1;
+                unit_coords(u, s, nt, mt, kb0, kb1);
+                const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
+                if (!wait_bounded(acce_bar(buf), use ^ 1u, p.wait_limit_ns, abort_flag,
+                                  kSiteMmaAccEmpty))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem_base + buf * BMS;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
+                                      kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t st = base + stage * G::kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk) {
+                        const uint64_t adesc = make_sdesc_sw128(st + kk * (UK * 128), kBSlab, 1024);
+                        const uint64_t bdesc = make_sdesc_sw128(st + kBTile + kk * (UK * 2), 16, 1024);
+                        umma_f16(d, adesc, bdesc, G::kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == (uint32_t)kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(accf_bar(buf));
+            }
+            umma_commit(drain_bar);
+            wait_drain(drain_bar, 0u, p.wait_limit_ns, abort_flag);
+        }
+    } else {
+        // ============================================================ epilogue
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int ethread = threadIdx.x - 64;        // 0 .. 127
+        int64_t i = 0;
+        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++i) {
+            int64_t s, nt, mt;
+            int kb0, kb1;
+            unit_coords(u, s, nt, mt, kb0, kb1);
+            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
+            const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
+                                         kSiteEpiAccFull);
+            if (!ok)
+                *abort_flag = 1u;
+            // The 128 epilogue threads meet at named barriers below, so they
+            // must all take the same decision: thread 0 reads the flag once.
+            epi_bar_sync();
+            if (ethread == 0)
+                *decision = *abort_flag;
+            epi_bar_sync();
+            if (*decision)
+                break;
+            tc_fence_after_sync();
+            const int64_t n = nt * BNT + 32 * q + lane;   // TMEM lane = output column
+            const int64_t m0 = mt * BMS;
+            float *part = p.part + (size_t)s * p.M * p.N;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BMS; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld_x16_sync(tmem_base + lane_base + buf * BMS + c0, r);
+                if (n < p.N) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int64_t m = m0 + c0 + c;
+                        if (m < p.M)
+                            __stcg(part + m * p.N + n, __uint_as_float(r[c]));
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce_bar(buf));
+
+            // publish this partial, then take a ticket for the tile
+            __threadfence();
+            epi_bar_sync();
+            if (ethread == 0) {
+                const int64_t tile = mt * p.n_tiles + nt;
+                *last_flag = ticket_arrive(p.tickets + tile, p.epoch, (uint32_t)p.splits, abort_flag);
+            }
+            epi_bar_sync();
+            const int last = *last_flag;
+            if (last == 1) {
+                __threadfence();
+                if (n < p.N) {
+#pragma unroll 1
+                    for (int c = 0; c < BMS; ++c) {
+                        const int64_t m = m0 + c;
+                        if (m >= p.M)
+                            break;
+                        float acc = 0.0f;
+                        for (int64_t ss = 0; ss < S; ++ss)
+                            acc += __ldcg(p.part + ((size_t)ss * p.M + m) * p.N + n);
+                        const __half h = __float2half_rn(fmaxf(acc, 0.0f));
+                        p.C[m * p.N + n] = *reinterpret_cast<const uint16_t *>(&h);
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, G::kTmemCols);
+    }
+}
+
+}  // namespace splitk
+
+}  // namespace gemmrelu
