@@ -35,7 +35,10 @@ METRIC = "GEMM+ReLU TFLOP/s (fp16 in, fp32 acc)"
 
 # DRAM bytes (read + write) per launch from ncu captures of the current
 # kernels, keyed by (kind, M, N, K); a shape missing here reports null.
-DRAM_BYTES_PER_LAUNCH = {}
+DRAM_BYTES_PER_LAUNCH = {
+    # profiles/gemm_relu_splitk_16x8192x8192.md: 134.623488 MB read + 3.639296 MB written
+    ("splitk", 16, 8192, 8192): 138262784,
+}
 
 
 def load_peaks():

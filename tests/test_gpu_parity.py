@@ -229,5 +229,9 @@ def test_error_growth_is_smooth(orc):
         o = orc.gemm_relu_f16(A, B).astype(np.float64)
         pos = o > 0
         rels.append(float(np.abs(g - o)[pos].mean() / np.sqrt(K)))
-    med = float(np.median(rels))
-    assert max(rels) <= 4 * med and max(rels) < 1e-3, rels
+    # smooth growth: at most 4x per doubling of K (with a floor for the many
+    # exact small-K cases), and far below what one dropped 64-wide k tile gives
+    # (a relative error of order 8 / sqrt(K), i.e. > 1e-2 here)
+    for a, b in zip(rels, rels[1:]):
+        assert b <= 4 * a + 1e-6, rels
+    assert max(rels) < 1e-4, rels
