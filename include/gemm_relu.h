@@ -18,8 +18,8 @@
  * ---------------------------------------
  *  - Pointers A, B, C and `workspace` are DEVICE pointers on the current CUDA
  *    device; the caller allocates and owns them.  The library allocates no
- *    memory per call.  Per device it keeps a few bytes of state (a status
- *    word) in a static device variable.
+ *    memory per call.  Per device it keeps a status word and the fixed
+ *    scratch array of gemm_relu_f16_splitk_noalloc in static device variables.
  *  - Pointers must be at least 2-byte aligned.  When A, B and C are 16-byte
  *    aligned and K and N are multiples of 8 (16-byte row pitches), operands
  *    move by TMA; otherwise by plain predicated loads and stores.  Both give
@@ -49,7 +49,9 @@ typedef enum {
     GEMMRELU_ERR_WORKSPACE = 3,          /* split_k < 1, or workspace null / smaller than the query */
     GEMMRELU_ERR_LAUNCH = 4,             /* CUDA reported an error configuring or launching a kernel */
     GEMMRELU_ERR_TIMEOUT = 5,            /* a bounded device-side wait expired (from gemm_relu_status) */
-    GEMMRELU_ERR_CUDA = 6                /* another CUDA runtime error (e.g. while reading the status) */
+    GEMMRELU_ERR_CUDA = 6,               /* another CUDA runtime error (e.g. while reading the status) */
+    GEMMRELU_ERR_SCRATCH_LIMIT = 7       /* gemm_relu_f16_splitk_noalloc: problem needs more scratch
+                                            than GEMMRELU_NOALLOC_SCRATCH_BYTES */
 } gemmrelu_status;
 
 /*
@@ -100,6 +102,47 @@ size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int
 int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
                          int64_t M, int64_t N, int64_t K, int split_k,
                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * gemm_relu_f16_splitk_noalloc -- gemm_relu_f16_splitk for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this entry point.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator -- for
+ * example a host framework that owns every byte of device memory through its
+ * own pool and forbids libraries to allocate behind its back, a serving loop
+ * that bans allocation after warm-up so its latency and footprint stay
+ * fixed, or a plugin that is handed only input and output pointers and has
+ * no way to obtain a workspace.  Such callers pass A, B and C exactly as for
+ * gemm_relu_f16_splitk; the split-K partial sums and per-tile counters live
+ * in a fixed scratch array compiled into this library instead of a caller
+ * workspace.  Nothing is allocated by this call.
+ *
+ * Scratch: GEMMRELU_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory in a
+ * static device array.  Every GPU that loads the library holds it until the
+ * process exits.  A problem needs
+ * gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes of it; larger
+ * problems are rejected with GEMMRELU_ERR_SCRATCH_LIMIT and nothing is
+ * launched.  (16 x 8192 x 8192 at split_k 8 needs 4 MiB + 512 B.)
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current.  Make that first call
+ * before any stream capture begins.  A failed look-up returns
+ * GEMMRELU_ERR_CUDA.
+ *
+ * Sharing: every call on a device uses the same array, and it keeps whatever
+ * the previous call left there.  The counters are tagged with a per-call
+ * number, so leftover contents are harmless and nothing needs clearing
+ * between calls.  Calls whose kernels may overlap on the GPU (for example on
+ * two streams without ordering between them) race on the array and give
+ * undefined results: order them on one stream or with events.
+ *
+ * Everything else -- arguments, layouts, alignment, the fallback to the
+ * unsplit kernel when split_k == 1 or the operands cannot use TMA, status
+ * reporting -- is as for gemm_relu_f16_splitk.
+ */
+#define GEMMRELU_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+int gemm_relu_f16_splitk_noalloc(const void *A, const void *B, void *C,
+                                 int64_t M, int64_t N, int64_t K, int split_k, void *stream);
 
 /*
  * gemm_relu_status -- synchronise `stream`, then return and clear the current

@@ -22,6 +22,8 @@ ERR_WORKSPACE = 3
 ERR_LAUNCH = 4
 ERR_TIMEOUT = 5
 ERR_CUDA = 6
+ERR_SCRATCH_LIMIT = 7
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 PATH_NONE, PATH_TMA, PATH_LSU = 0, 1, 2
 
@@ -50,6 +52,8 @@ def lib():
         L.gemm_relu_f16_splitk_workspace_bytes.restype = sz
         L.gemm_relu_f16_splitk.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
         L.gemm_relu_f16_splitk.restype = i32
+        L.gemm_relu_f16_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_relu_f16_splitk_noalloc.restype = i32
         L.gemm_relu_status.argtypes = [vp]
         L.gemm_relu_status.restype = i32
         L.gemm_relu_strerror.argtypes = [i32]
@@ -79,6 +83,12 @@ def gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k):
 def gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, workspace, workspace_bytes, stream=None):
     return lib().gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, workspace, workspace_bytes,
                                       stream)
+
+
+def gemm_relu_f16_splitk_noalloc(A, B, C, M, N, K, split_k, stream=None):
+    """Split-K without a caller workspace, for callers that may not allocate
+    device memory; uses the library's fixed 8 MiB device scratch array."""
+    return lib().gemm_relu_f16_splitk_noalloc(A, B, C, M, N, K, split_k, stream)
 
 
 def gemm_relu_status(stream=None):

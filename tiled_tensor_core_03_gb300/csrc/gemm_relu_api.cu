@@ -258,6 +258,32 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
     return launch_status(cudaGetLastError());
 }
 
+// ---------------------------------------------------------------- no-alloc scratch
+// Split-K scratch for gemm_relu_f16_splitk_noalloc: a fixed array in every
+// device's copy of this module, so callers that cannot allocate still get a
+// workspace.  Host code must not use the symbol's host-side name as a device
+// address; it looks the address up once per device instead.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMMRELU_NOALLOC_SCRATCH_BYTES];
+
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on the
+// first call per device, with that device current).
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return GEMMRELU_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return GEMMRELU_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMMRELU_OK;
+}
+
 }  // namespace
 
 // ==================================================================== C ABI
@@ -323,6 +349,28 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C, int64_t M, int64
     }
 }
 
+int gemm_relu_f16_splitk_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
+                                 int64_t K, int split_k, void *stream) {
+    int rc = check_args(A, B, C, M, N, K);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    if (split_k < 1)
+        return GEMMRELU_ERR_WORKSPACE;
+    if (M == 0 || N == 0)
+        return GEMMRELU_OK;
+    const size_t need = gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k);
+    if (need > GEMMRELU_NOALLOC_SCRATCH_BYTES)
+        return GEMMRELU_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (need > 0) {
+        rc = noalloc_scratch(&scratch);
+        if (rc != GEMMRELU_OK)
+            return rc;
+    }
+    return gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, scratch,
+                                need > 0 ? GEMMRELU_NOALLOC_SCRATCH_BYTES : 0, stream);
+}
+
 int gemm_relu_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return GEMMRELU_ERR_CUDA;
@@ -343,6 +391,8 @@ const char *gemm_relu_strerror(int code) {
     case GEMMRELU_ERR_LAUNCH: return "CUDA error configuring or launching a kernel";
     case GEMMRELU_ERR_TIMEOUT: return "a bounded device-side wait expired";
     case GEMMRELU_ERR_CUDA: return "CUDA runtime error";
+    case GEMMRELU_ERR_SCRATCH_LIMIT:
+        return "split-K scratch needed exceeds the built-in GEMMRELU_NOALLOC_SCRATCH_BYTES buffer";
     default: return "unknown status";
     }
 }
