@@ -78,26 +78,28 @@ size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int
  * gemm_relu_f16_splitk -- the same C = fp16(max(A . B, 0)), with the K range
  * cut into `split_k` contiguous pieces computed by different CTAs.
  *
- * Follows the split-K scheme of "TileLang 编程基本知识点" section 5.1 (grid
- * axis over K pieces, each piece offsets only K), taking that page's advice
- * for reproducibility: instead of fp32 atomic adds into C, every piece writes
- * its raw fp32 partial to `workspace`, and the last piece to finish a tile
- * (found with a per-tile arrival counter in the workspace) sums the partials
- * in the fixed order 0..split_k-1, applies ReLU and writes fp16 C.  Results
- * are therefore bit-identical from run to run.  ReLU is never applied to a
- * partial sum.
+ * Follows the split-K scheme of "TileLang 编程基本知识点" section 5.1 (work
+ * split over K pieces, each piece offsetting only K) with that page's advice
+ * for reproducible results: instead of fp32 atomic adds into C, the call runs
+ * two stages on `stream`.  Stage 1 computes each piece's raw fp32 partial
+ * (no ReLU) into `workspace`; stage 2 sums the partials in the fixed order
+ * 0..split_k-1, applies ReLU and writes fp16 C.  Results are bit-identical
+ * from run to run.  Stage 2 is a programmatic dependent launch of stage 1, so
+ * it needs no host synchronisation between them.
  *
  * The product is computed as C^T = B^T . A^T so that small M maps onto the
  * narrow (N) side of the MMA; this suits skinny, memory-bound shapes.
  *
- * split_k  : >= 1.  Values above ceil(K / 64) are clamped to it.
+ * split_k  : >= 1.  K is processed in stages of 64, 128 or 256 k (256 when
+ *            M <= 32); split_k is clamped to the number of such stages.
  * workspace: device buffer of at least
- *            gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes,
- *            16-byte aligned.  Its contents need no initialisation; calls that
- *            may run concurrently on the GPU must use distinct workspaces.
+ *            gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes
+ *            (split_k * M * N fp32 partials), 16-byte aligned.  Its contents
+ *            need no initialisation; calls that may run concurrently on the
+ *            GPU must use distinct workspaces.
  * Needs A, B 16-byte aligned with K and N multiples of 8 (TMA operands);
- * otherwise, or when split_k == 1, the call runs gemm_relu_f16's kernel and
- * leaves the workspace untouched.
+ * otherwise, or when the clamped split_k is 1, the call runs gemm_relu_f16's
+ * kernel and leaves the workspace untouched.
  */
 int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
                          int64_t M, int64_t N, int64_t K, int split_k,
@@ -113,16 +115,16 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
  * that bans allocation after warm-up so its latency and footprint stay
  * fixed, or a plugin that is handed only input and output pointers and has
  * no way to obtain a workspace.  Such callers pass A, B and C exactly as for
- * gemm_relu_f16_splitk; the split-K partial sums and per-tile counters live
- * in a fixed scratch array compiled into this library instead of a caller
- * workspace.  Nothing is allocated by this call.
+ * gemm_relu_f16_splitk; the split-K partial sums live in a fixed scratch
+ * array compiled into this library instead of a caller workspace.  Nothing
+ * is allocated by this call.
  *
  * Scratch: GEMMRELU_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory in a
  * static device array.  Every GPU that loads the library holds it until the
  * process exits.  A problem needs
  * gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes of it; larger
  * problems are rejected with GEMMRELU_ERR_SCRATCH_LIMIT and nothing is
- * launched.  (16 x 8192 x 8192 at split_k 8 needs 4 MiB + 512 B.)
+ * launched.  (16 x 8192 x 8192 at split_k 8 needs 4 MiB.)
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current.  Make that first call
@@ -130,11 +132,11 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
  * GEMMRELU_ERR_CUDA.
  *
  * Sharing: every call on a device uses the same array, and it keeps whatever
- * the previous call left there.  The counters are tagged with a per-call
- * number, so leftover contents are harmless and nothing needs clearing
- * between calls.  Calls whose kernels may overlap on the GPU (for example on
- * two streams without ordering between them) race on the array and give
- * undefined results: order them on one stream or with events.
+ * the previous call left there.  Every byte a call reads from it is first
+ * written by the same call, so leftover contents are harmless and nothing
+ * needs clearing between calls.  Calls whose kernels may overlap on the GPU
+ * (for example on two streams without ordering between them) race on the
+ * array and give undefined results: order them on one stream or with events.
  *
  * Everything else -- arguments, layouts, alignment, the fallback to the
  * unsplit kernel when split_k == 1 or the operands cannot use TMA, status

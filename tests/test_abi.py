@@ -94,10 +94,14 @@ def test_rasteriser_panel_order(lib):
 
 
 def test_splitk_workspace_size(lib):
-    # 16 x 8192 x 8192, split 8: tickets (64 tiles x 8 B, rounded to 256 B) + 8 x 16 x 8192 fp32
-    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 8) == 512 + 8 * 16 * 8192 * 4
+    # split_k * M * N fp32 partials
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 8) == 8 * 16 * 8192 * 4
     assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 1) == 0
-    # split clamped to the number of 64-wide k blocks
-    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 128, 100, 8) == 256 + 2 * 16 * 128 * 4
+    # M <= 32 works in 256-wide k stages: K = 600 has 3, so split 8 clamps to 3
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 128, 600, 8) == 3 * 16 * 128 * 4
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 128, 100, 8) == 0     # one stage
+    # 32 < M <= 64 works in 128-wide stages, larger M in 64-wide ones
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(64, 128, 600, 8) == 5 * 64 * 128 * 4
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(200, 128, 600, 16) == 10 * 200 * 128 * 4
     assert gr.gemm_relu_f16_splitk_workspace_bytes(0, 8, 8, 2) == 0
     assert gr.gemm_relu_f16_splitk_workspace_bytes(8, 8, 8, 0) == 0

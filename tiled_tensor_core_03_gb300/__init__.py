@@ -171,8 +171,9 @@ def splitk_workspace(M, N, K, split_k, device=None):
 
 
 def gemm_relu_splitk(a, b, split_k, out=None, workspace=None, stream=None):
-    """Same result as gemm_relu, with K split into `split_k` pieces and a
-    deterministic in-kernel reduction (for skinny, memory-bound shapes)."""
+    """Same result as gemm_relu, with K split into `split_k` pieces whose fp32
+    partials are reduced in fixed order by a second kernel (for skinny,
+    memory-bound shapes; bit-reproducible)."""
     _check_operands(a, b)
     c = _out(a, b, out)
     M, K = a.shape

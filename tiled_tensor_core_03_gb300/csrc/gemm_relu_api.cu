@@ -4,7 +4,8 @@
 // encoding (CUDA driver entry point fetched through the runtime, so the
 // library needs no link against libcuda), launch configuration and the
 // device status word.  Every arithmetic step runs in the kernels of
-// gemm_relu_kernels.cuh; there is no host or library fallback.
+// gemm_relu_kernels.cuh and gemm_relu_splitk.cuh; there is no host or library
+// fallback.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -16,19 +17,26 @@
 
 #include "gemm_relu.h"
 #include "gemm_relu_kernels.cuh"
+#include "gemm_relu_splitk.cuh"
 
 namespace {
 
 using gemmrelu::tile_coord;
 
 constexpr int64_t kMaxDim = 0x7fffffff;
-constexpr int kPanel = 8;                       // M blocks per rasteriser panel
+#ifndef GEMMRELU_PANEL
+#define GEMMRELU_PANEL 8
+#endif
+#ifndef GEMMRELU_SPLIT_MAJOR
+#define GEMMRELU_SPLIT_MAJOR 1
+#endif
+constexpr int kPanel = GEMMRELU_PANEL;             // M blocks per rasteriser panel
+constexpr int kSplitMajor = GEMMRELU_SPLIT_MAJOR;  // split-K work-unit order
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- test hooks
 std::atomic<int> g_drop_arrive{0};
 std::atomic<int64_t> g_wait_limit_ns{0};
-std::atomic<uint32_t> g_epoch{0};
 
 uint64_t wait_limit_ns() {
     const int64_t v = g_wait_limit_ns.load();
@@ -203,25 +211,53 @@ int split_bms(int64_t M) {
     return 128;
 }
 
-int effective_splits(int64_t K, int split_k) {
-    const int64_t num_kb = (K + S::BK - 1) / S::BK;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(split_k, num_kb));
+// k per pipeline stage of the split-K kernel instantiated for `bms`.
+int64_t split_super_k(int bms) { return (int64_t)S::BK * S::kbs_for(bms); }
+
+int64_t split_super_blocks(int64_t K, int bms) {
+    return (K + split_super_k(bms) - 1) / split_super_k(bms);
+}
+
+int effective_splits(int64_t K, int bms, int split_k) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(split_k, split_super_blocks(K, bms)));
 }
 
 struct SplitLayout {
     int bms, splits;
-    int64_t n_tiles, m_tiles, tickets_bytes, part_bytes;
+    int64_t n_tiles, m_tiles, part_bytes;
 };
 
 SplitLayout split_layout(int64_t M, int64_t N, int64_t K, int split_k) {
     SplitLayout L{};
     L.bms = split_bms(M);
-    L.splits = effective_splits(K, split_k);
+    L.splits = effective_splits(K, L.bms, split_k);
     L.n_tiles = (N + S::BNT - 1) / S::BNT;
     L.m_tiles = (M + L.bms - 1) / L.bms;
-    L.tickets_bytes = ((L.n_tiles * L.m_tiles * 8 + 255) / 256) * 256;
     L.part_bytes = (int64_t)L.splits * M * N * 4;
     return L;
+}
+
+// Stage 2 launch: programmatic dependent of the partial kernel just queued on
+// `stream`, so its CTAs can become resident while stage 1 drains.
+int launch_split_reduce(const float *part, void *C, int64_t M, int64_t N, int splits,
+                        cudaStream_t stream, DeviceState *ds) {
+    const int64_t groups = M * (N / 8);
+    const int64_t blocks = std::max<int64_t>(
+        1, std::min<int64_t>((groups + 255) / 256, (int64_t)4 * ds->sms));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int c_vec16 = aligned(C, 16) ? 1 : 0;
+    return launch_status(cudaLaunchKernelEx(&cfg, S::gemm_relu_splitk_reduce_kernel, part,
+                                            static_cast<uint16_t *>(C), (int)M, (int)N, splits,
+                                            c_vec16));
 }
 
 template <int BMS>
@@ -230,32 +266,30 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
                      bool &attr_done) {
     using G = S::Cfg<BMS>;
     S::Params p{};
-    p.C = static_cast<uint16_t *>(C);
-    p.tickets = static_cast<unsigned long long *>(ws);
-    p.part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.tickets_bytes);
+    p.part = static_cast<float *>(ws);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
-    p.num_kb = (int)((K + S::BK - 1) / S::BK);
+    p.num_sb = (int)split_super_blocks(K, BMS);
     p.splits = L.splits;
     p.n_tiles = L.n_tiles;
     p.m_tiles = L.m_tiles;
     p.num_units = L.n_tiles * L.m_tiles * L.splits;
-    uint32_t e = ++g_epoch;
-    if (e == 0)
-        e = ++g_epoch;
-    p.epoch = e;
+    p.split_major = kSplitMajor;
     p.drop_arrive = g_drop_arrive.load();
     p.wait_limit_ns = wait_limit_ns();
     CUtensorMap mA, mB;
-    if (!make_map(&mA, A, M, K, S::BK, BMS) || !make_map(&mB, B, K, N, 64, S::BK))
+    if (!make_map(&mA, A, M, K, S::BK, BMS) || !make_map(&mB, B, K, N, 64, G::kSuperK))
         return GEMMRELU_ERR_LAUNCH;
-    auto kern = S::gemm_relu_splitk_kernel<BMS>;
+    auto kern = S::gemm_relu_splitk_partial_kernel<BMS>;
     if (!ensure_smem_attr(attr_done, kern, G::kSmemBytes))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t grid = std::min<int64_t>(p.num_units, ds->sms);
     kern<<<(unsigned)grid, 192, G::kSmemBytes, stream>>>(mA, mB, p);
-    return launch_status(cudaGetLastError());
+    const int rc = launch_status(cudaGetLastError());
+    if (rc != GEMMRELU_OK)
+        return rc;
+    return launch_split_reduce(p.part, C, M, N, L.splits, stream, ds);
 }
 
 // ---------------------------------------------------------------- no-alloc scratch
@@ -312,7 +346,7 @@ size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int
     const SplitLayout L = split_layout(M, N, K, split_k);
     if (L.splits <= 1)
         return 0;
-    return (size_t)(L.tickets_bytes + L.part_bytes);
+    return (size_t)L.part_bytes;
 }
 
 int gemm_relu_f16_splitk(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -334,7 +368,7 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C, int64_t M, int64
     const SplitLayout L = split_layout(M, N, K, split_k);
     if (L.splits <= 1 || !tma_ok(A, K) || !tma_ok(B, N))
         return launch_fused(A, B, C, M, N, K, s, ds);
-    const size_t need = (size_t)(L.tickets_bytes + L.part_bytes);
+    const size_t need = (size_t)L.part_bytes;
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
         return GEMMRELU_ERR_WORKSPACE;
     switch (L.bms) {

@@ -50,7 +50,6 @@ enum WaitSite : unsigned {
     kSiteMmaFull = 3,
     kSiteEpiAccFull = 4,
     kSiteDrain = 5,
-    kSiteTicket = 6,
 };
 
 __device__ __forceinline__ void record_timeout(volatile uint32_t *abort_flag, unsigned where) {
@@ -518,302 +517,5 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
 
 }  // namespace fused
 
-// ================================================================== split-K kernel
-//
-// C^T = B^T . A^T per K piece: the MMA's M side (128 TMEM lanes) runs over N
-// and its narrow N side (BMS columns) over M, so M = 16 costs a 128 x 16 MMA
-// instead of a 128-row tile mostly empty.  UMMA A operand = a B tile,
-// N-major; UMMA B operand = an A tile, K-major.  Each work unit (n tile,
-// m tile, split s) accumulates k blocks [s*kb/S, (s+1)*kb/S) and writes its
-// raw fp32 partial to the workspace; the last unit of a tile to finish (an
-// arrival counter per tile, tagged with the call's epoch) sums the S
-// partials in order 0..S-1, applies ReLU, rounds to fp16 and writes C.
-
-namespace splitk {
-
-constexpr int BNT = 128;                     // N per tile (UMMA M)
-constexpr int BK = 64;
-constexpr int UK = 16;
-constexpr uint32_t kBSlab = BK * 64 * 2;     // 8 KB
-constexpr uint32_t kBTile = BK * BNT * 2;    // 16 KB = 2 slabs
-constexpr int kEpiWarps = 4;
-
-template <int BMS>
-struct Cfg {
-    static constexpr uint32_t kATile = BMS * BK * 2;            // K-major, BMS rows
-    static constexpr uint32_t kStageBytes = kBTile + kATile;
-    static constexpr uint32_t kBudget = 227u * 1024u - 1024u - 256u;
-    static constexpr int kStagesRaw = (int)(kBudget / kStageBytes);
-    static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-    static constexpr uint32_t kOffBar = kStages * kStageBytes;
-    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
-    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
-    static constexpr uint32_t kTmemCols = (2 * BMS < 32) ? 32 : 2 * BMS;  // power of 2
-    // UMMA A (the B tile) N-major: bit 15 = 1; UMMA B (the A tile) K-major.
-    static constexpr uint32_t kIdesc = make_idesc_f16_f32(BNT, BMS, 1, 0);
-};
-
-struct Params {
-    uint16_t *C;
-    float *part;                       // [S][M][N] fp32
-    unsigned long long *tickets;       // [m_tiles * n_tiles]
-    int M, N, K;
-    int num_kb, splits;
-    int64_t n_tiles, m_tiles, num_units;
-    uint32_t epoch;
-    int drop_arrive;
-    uint64_t wait_limit_ns;
-};
-
-// Per-tile arrival counter: word = (epoch << 32) | count.  A word carrying
-// another epoch (stale, or never used) counts as zero.  The arrival that
-// brings the count to `splits` is the last; it resets the word to 0.
-__device__ __forceinline__ int ticket_arrive(unsigned long long *w, uint32_t epoch,
-                                             uint32_t splits, volatile uint32_t *abort_flag) {
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(w);
-    for (int it = 0; it < (1 << 20); ++it) {
-        const uint32_t e = (uint32_t)(old >> 32);
-        const uint32_t c = (uint32_t)old;
-        const uint32_t nc = (e == epoch) ? c + 1u : 1u;
-        const unsigned long long nw =
-            (nc >= splits) ? 0ull : (((unsigned long long)epoch << 32) | nc);
-        const unsigned long long prev = atomicCAS(w, old, nw);
-        if (prev == old)
-            return nc >= splits ? 1 : 0;
-        old = prev;
-    }
-    record_timeout(abort_flag, kSiteTicket);
-    return -1;
-}
-
-__device__ __forceinline__ void epi_bar_sync() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-template <int BMS>
-__global__ void __launch_bounds__(192, 1)
-    gemm_relu_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const Params p) {
-    using G = Cfg<BMS>;
-    constexpr int kStages = G::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_addr(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
-
-    const uint32_t bar0 = base + G::kOffBar;
-    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kStages + s); };
-    auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
-    auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + G::kOffMisc);
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 4);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(gbase + G::kOffMisc + 8);
-    volatile uint32_t *decision = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 12);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t S = p.splits;
-
-    if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
-            mbar_init(full_bar(s), 1u);
-            mbar_init(empty_bar(s), 1u);
-        }
-        for (uint32_t b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), 1u);
-            mbar_init(acce_bar(b), (uint32_t)kEpiWarps);
-        }
-        mbar_init(drain_bar, 1u);
-        *abort_flag = 0u;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tmA);
-        tma_prefetch_map(&tmB);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), G::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
-
-    auto unit_coords = [&](int64_t u, int64_t &s, int64_t &nt, int64_t &mt, int &kb0, int &kb1) {
-        s = u % S;
-        const int64_t tile = u / S;
-        nt = tile % p.n_tiles;
-        mt = tile / p.n_tiles;
-        kb0 = (int)((s * p.num_kb) / S);
-        kb1 = (int)(((s + 1) * p.num_kb) / S);
-    };
-
-    if (warp == 0) {
-        // ============================================================ TMA producer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, parity = 0, issued = 0;
-            bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-                int64_t s, nt, mt;
-                int kb0, kb1;
-                unit_coords(u, s, nt, mt, kb0, kb1);
-                const int n0 = (int)(nt * BNT), m0 = (int)(mt * BMS);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
-                                      kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const bool drop = p.drop_arrive && blockIdx.x == 0 && u == blockIdx.x && kb == kb0;
-                    if (!drop) {
-                        const uint32_t fb = full_bar(stage);
-                        const uint32_t dst = base + stage * G::kStageBytes;
-                        mbar_arrive_expect_tx(fb, G::kStageBytes);
-                        tma_load_2d(&tmB, dst, fb, n0, kb * BK);
-                        tma_load_2d(&tmB, dst + kBSlab, fb, n0 + 64, kb * BK);
-                        tma_load_2d(&tmA, dst + kBTile, fb, kb * BK, m0);
-                        issued |= 1u << stage;
-                        parity = (parity & ~(1u << stage)) | (phase << stage);
-                    }
-                    if (++stage == (uint32_t)kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            for (uint32_t s = 0; s < (uint32_t)kStages; ++s)
-                if (issued & (1u << s))
-                    wait_drain(full_bar(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
-        }
-    } else if (warp == 1) {
-        // ============================================================ MMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            int64_t i = 0;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++i) {
-                int64_t s, nt, mt;
-                int kb0, kb1;
-                unit_coords(u, s, nt, mt, kb0, kb1);
-                const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
-                if (!wait_bounded(acce_bar(buf), use ^ 1u, p.wait_limit_ns, abort_flag,
-                                  kSiteMmaAccEmpty))
-                    break;
-                tc_fence_after_sync();
-                const uint32_t d = tmem_base + buf * BMS;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
-                                      kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t st = base + stage * G::kStageBytes;
-#pragma unroll
-                    for (int kk = 0; kk < BK / UK; ++kk) {
-                        const uint64_t adesc = make_sdesc_sw128(st + kk * (UK * 128), kBSlab, 1024);
-                        const uint64_t bdesc = make_sdesc_sw128(st + kBTile + kk * (UK * 2), 16, 1024);
-                        umma_f16(d, adesc, bdesc, G::kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(empty_bar(stage));
-                    if (++stage == (uint32_t)kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok)
-                    break;
-                umma_commit(accf_bar(buf));
-            }
-            umma_commit(drain_bar);
-            wait_drain(drain_bar, 0u, p.wait_limit_ns, abort_flag);
-        }
-    } else {
-        // ============================================================ epilogue
-        const int q = warp & 3;
-        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const int ethread = threadIdx.x - 64;        // 0 .. 127
-        int64_t i = 0;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++i) {
-            int64_t s, nt, mt;
-            int kb0, kb1;
-            unit_coords(u, s, nt, mt, kb0, kb1);
-            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
-            const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
-                                         kSiteEpiAccFull);
-            if (!ok)
-                *abort_flag = 1u;
-            // The 128 epilogue threads meet at named barriers below, so they
-            // must all take the same decision: thread 0 reads the flag once.
-            epi_bar_sync();
-            if (ethread == 0)
-                *decision = *abort_flag;
-            epi_bar_sync();
-            if (*decision)
-                break;
-            tc_fence_after_sync();
-            const int64_t n = nt * BNT + 32 * q + lane;   // TMEM lane = output column
-            const int64_t m0 = mt * BMS;
-            float *part = p.part + (size_t)s * p.M * p.N;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BMS; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld_x16_sync(tmem_base + lane_base + buf * BMS + c0, r);
-                if (n < p.N) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int64_t m = m0 + c0 + c;
-                        if (m < p.M)
-                            __stcg(part + m * p.N + n, __uint_as_float(r[c]));
-                    }
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(acce_bar(buf));
-
-            // publish this partial, then take a ticket for the tile
-            __threadfence();
-            epi_bar_sync();
-            if (ethread == 0) {
-                const int64_t tile = mt * p.n_tiles + nt;
-                *last_flag = ticket_arrive(p.tickets + tile, p.epoch, (uint32_t)p.splits, abort_flag);
-            }
-            epi_bar_sync();
-            const int last = *last_flag;
-            if (last == 1) {
-                __threadfence();
-                if (n < p.N) {
-#pragma unroll 1
-                    for (int c = 0; c < BMS; ++c) {
-                        const int64_t m = m0 + c;
-                        if (m >= p.M)
-                            break;
-                        float acc = 0.0f;
-                        for (int64_t ss = 0; ss < S; ++ss)
-                            acc += __ldcg(p.part + ((size_t)ss * p.M + m) * p.N + n);
-                        const __half h = __float2half_rn(fmaxf(acc, 0.0f));
-                        p.C[m * p.N + n] = *reinterpret_cast<const uint16_t *>(&h);
-                    }
-                }
-            }
-        }
-    }
-
-    __syncwarp();
-    tc_fence_before_sync();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after_sync();
-        tmem_dealloc(tmem_base, G::kTmemCols);
-    }
-}
-
-}  // namespace splitk
 
 }  // namespace gemmrelu
