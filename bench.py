@@ -2,7 +2,8 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
   1. the fused kernel on M = N = K = 4096 (A, B ~ N(0,1)/sqrt(K)): tile
-     rasteriser, TMA ring, tcgen05 MMA into TMEM, ReLU/fp16 epilogue;
+     rasteriser, TMA ring, tcgen05 MMA into TMEM, ReLU/fp16 epilogue, with
+     the stream-K schedule for the partial last wave;
   2. the split-K kernel on M = 16, N = K = 8192 (N(0,1)/sqrt(K)), split 8:
      fp32 partials to the workspace, then a fixed-order reduce + ReLU kernel.
 Metric: GEMM+ReLU TFLOP/s = total 2*M*N*K of the step / step time.
@@ -65,18 +66,22 @@ def describe(w):
 
 
 def build_parts(args):
-    """[(label, workload, kind)], description.  kind: 'fused' or 'splitk'."""
+    """[(label, workload, kind)], description.  kind: 'streamk' (the fused
+    kernel through gemm_relu_streamk, which runs plain data-parallel tiles when
+    the schedule has no cut), 'fused' or 'splitk'."""
     from tiled_tensor_core_03_gb300 import inputs
     W = inputs.WORKLOADS
     if args.shape:
         M, N, K = (int(x) for x in args.shape.lower().split("x"))
         w = inputs.Workload("custom", M, N, K, "normal", True, 7, split_k=args.split)
-        return [("custom", w, "splitk" if args.split > 1 else "fused")], describe(w)
+        kind = "splitk" if args.split > 1 else ("fused" if args.no_streamk else "streamk")
+        return [("custom", w, kind)], describe(w)
     if args.workload == "step":
-        return [("fused_4096", W["square4096"], "fused"),
+        return [("fused_4096", W["square4096"], "streamk"),
                 ("splitk_skinny", W["skinny"], "splitk")], STEP_NAME
     w = W[args.workload]
-    return [(w.name, w, "splitk" if w.split_k > 1 else "fused")], describe(w)
+    kind = "splitk" if w.split_k > 1 else ("fused" if args.no_streamk else "streamk")
+    return [(w.name, w, kind)], describe(w)
 
 
 # ------------------------------------------------------------------ clocks
@@ -264,7 +269,8 @@ def run_ours(args, world, rank, local):
         a = torch.from_numpy(A).to(device)
         b = torch.from_numpy(B).to(device)
         c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
-        ws = gr.splitk_workspace(w.M, w.N, w.K, w.split_k, device) if kind == "splitk" else None
+        ws = (gr.splitk_workspace(w.M, w.N, w.K, w.split_k, device) if kind == "splitk" else
+              gr.streamk_workspace(w.M, w.N, w.K, device) if kind == "streamk" else None)
         dev[label] = (a, b, c, ws)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     clean = torch.ones(L2_CLEAN_BYTES, dtype=torch.uint8, device=device)
@@ -282,6 +288,8 @@ def run_ours(args, world, rank, local):
         a, b, c, ws = dev[label]
         if kind == "splitk":
             gr.gemm_relu_splitk(a, b, w.split_k, out=c, workspace=ws, stream=stream)
+        elif kind == "streamk":
+            gr.gemm_relu_streamk(a, b, out=c, workspace=ws, stream=stream)
         else:
             gr.gemm_relu(a, b, out=c, stream=stream)
 
@@ -369,8 +377,10 @@ def run_ours(args, world, rank, local):
 
     def roofline(label, w, kind):
         ms = statistics.mean(part_ms[label])
-        kernel = (f"gemm_relu_splitk_kernel {w.M}x{w.N}x{w.K} split {w.split_k}"
-                  if kind == "splitk" else f"gemm_relu_fused_kernel {w.M}x{w.N}x{w.K}")
+        kernel = (f"gemm_relu_splitk_partial+reduce {w.M}x{w.N}x{w.K} split {w.split_k}"
+                  if kind == "splitk" else
+                  f"gemm_relu_fused_kernel {w.M}x{w.N}x{w.K}"
+                  + (" (stream-K schedule)" if kind == "streamk" else ""))
         if w.flops / w.bytes >= ridge:
             ach = w.flops / (ms * 1e-3) / 1e12
             return {"bound": "tensor", "kernel": kernel, "achieved": ach, "peak": tensor_peak,
@@ -418,7 +428,7 @@ def run_ours(args, world, rank, local):
         "wall_ms_per_step_incl_flush": 1e3 * (wall1 - wall0) / args.steps,
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "tiled_tensor_core_03_gb300.gemm_relu / gemm_relu_splitk from pinned host buffers"},
+                "api": "tiled_tensor_core_03_gb300.gemm_relu_streamk / gemm_relu_splitk from pinned host buffers"},
         # this library's kernels in the timed region: the fused kernel once,
         # split-K as its partial and reduce kernels
         "gpu_launches": sum(2 if kind == "splitk" else 1 for _, _, kind in parts) * args.steps,
@@ -457,6 +467,8 @@ def main(argv=None):
                     choices=["step", "square256", "square1024", "ragged", "square4096", "skinny"])
     ap.add_argument("--shape", default=None, help="MxNxK: one custom fused (or split) GEMM")
     ap.add_argument("--split", type=int, default=1, help="split-K for --shape")
+    ap.add_argument("--no-streamk", action="store_true",
+                    help="time the plain data-parallel fused kernel instead of the stream-K call")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     world, rank, local = dist_env()

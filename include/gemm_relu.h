@@ -59,13 +59,50 @@ typedef enum {
  *
  * One fused kernel: TMA (or predicated loads) into a multistage shared-memory
  * ring, tcgen05.mma into a TMEM fp32 accumulator, ReLU + fp16 cast in the
- * epilogue, TMA (or predicated) stores.  Tiles of 128 x 256 outputs, a
- * persistent grid of at most one CTA per SM, grouped (L2-friendly) tile order.
+ * epilogue, TMA (or predicated) stores.  Tiles of 128 x 256 outputs (128 x
+ * 128 when that fills the SMs in fewer waves, e.g. 1024^3), a persistent grid
+ * of at most one CTA per SM, grouped (L2-friendly) tile order.
  *
  * Returns GEMMRELU_OK or an error code; asynchronous on `stream`.
  */
 int gemm_relu_f16(const void *A, const void *B, void *C,
                   int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * gemm_relu_f16_streamk_workspace_bytes -- bytes of device workspace that
+ * gemm_relu_f16_streamk needs for these sizes on the current device (its SM
+ * count decides the schedule); 0 when the call would run no stream-K part,
+ * for invalid arguments, or when no CUDA device is available.
+ */
+size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * gemm_relu_f16_streamk -- C = fp16(max(A . B, 0)) like gemm_relu_f16, with a
+ * stream-K schedule for the tiles of the last, partial wave.
+ *
+ * "TileLang tutorial" (chapter "Persistent kernel") names the problem: when
+ * the number of output tiles is not a multiple of the number of SMs, the
+ * last wave runs on part of the GPU only; stream-K splits the remaining work
+ * over all CTAs along K.  Here all full waves but the last run data-parallel
+ * (one 128 x 256 tile per CTA at a time); the k blocks of the remaining
+ * tiles are divided into one equal contiguous range per CTA.  A tile cut
+ * between two CTAs is finished by the CTA holding its first k blocks, which
+ * adds the other CTA's fp32 piece (passed through `workspace`) before the
+ * ReLU and the fp16 store.  Each tile is cut at most once, so the result is
+ * the same from run to run.
+ *
+ * workspace: device buffer of at least
+ *            gemm_relu_f16_streamk_workspace_bytes(M, N, K) bytes, 16-byte
+ *            aligned; its contents need no initialisation.  Calls that may
+ *            run concurrently on the GPU must use distinct workspaces.
+ * The launch is cooperative (all CTAs resident at once); it fails with
+ * GEMMRELU_ERR_LAUNCH if the GPU cannot host the whole grid.  When the
+ * tiles already fill whole waves, or the operands cannot use TMA, the call
+ * runs gemm_relu_f16's kernel and leaves the workspace untouched.
+ */
+int gemm_relu_f16_streamk(const void *A, const void *B, void *C,
+                          int64_t M, int64_t N, int64_t K,
+                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * gemm_relu_f16_splitk_workspace_bytes -- bytes of device workspace that
@@ -188,6 +225,17 @@ int gemm_relu_tile_coord(int64_t tile, int64_t m_tiles, int64_t n_tiles, int pan
  * Affects the calling process only.  Returns GEMMRELU_OK.
  */
 int gemm_relu_debug_set(int drop_arrive, int64_t wait_limit_ns);
+
+/*
+ * gemm_relu_debug_force_kernel -- test hook.  Selects the kernel that
+ * gemm_relu_f16 (and the unsplit fallbacks of the other entry points) runs:
+ * 0 = automatic choice (default), 1 = one CTA per 128 x 256 tile, 2 = one CTA
+ * per 128 x 128 tile, 3 = CTA pairs on 256 x 256 tiles (TMA operands only;
+ * others take the one-CTA kernel).  All give results within the same
+ * tolerance.  Affects the calling process only.  Returns GEMMRELU_OK, or
+ * GEMMRELU_ERR_INVALID_ARG for another value.
+ */
+int gemm_relu_debug_force_kernel(int which);
 
 #ifdef __cplusplus
 }

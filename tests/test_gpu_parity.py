@@ -235,3 +235,104 @@ def test_error_growth_is_smooth(orc):
     for a, b in zip(rels, rels[1:]):
         assert b <= 4 * a + 1e-6, rels
     assert max(rels) < 1e-4, rels
+
+
+# ----------------------------------------------------------------- stream-K
+
+
+def _sampled_parity(orc, A, B, got, what, seed=7):
+    M, K = A.shape
+    N = B.shape[1]
+    rows = sorted({r for mb in range((M + 127) // 128) for r in (mb * 128, min(M - 1, mb * 128 + 127))})
+    for r0 in range(0, len(rows), 16):
+        rr = rows[r0:r0 + 16]
+        want = np.concatenate([orc.gemm_relu_f16_rows(A, B, r, 1) for r in rr])
+        assert_parity(got[rr], want, abs_dot(A[rr], B), K, (what, "rows", rr[0]))
+    rng = np.random.default_rng(seed)
+    I = rng.integers(0, M, 2048)
+    J = rng.integers(0, N, 2048)
+    assert_parity(got[I, J], orc.gemm_relu_f16_at(A, B, I, J), abs_dot(A, B, I, J), K, (what, "samples"))
+
+
+STREAMK_SHAPES = [(4096, 4096, 4096), (2048, 5120, 320), (2000, 4104, 776), (3000, 4352, 64)]
+
+
+@pytest.fixture
+def one_cta():
+    """The single-CTA kernel (where the stream-K schedule lives)."""
+    gr.gemm_relu_debug_force_kernel(1)
+    yield
+    gr.gemm_relu_debug_force_kernel(0)
+
+
+@pytest.mark.parametrize("M,N,K", STREAMK_SHAPES)
+def test_streamk_parity(orc, one_cta, M, N, K):
+    import torch
+    assert gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K) > 0, "shape has no stream-K part"
+    A, B = inputs.make(M, N, K, "normal", True, seed=M + N + K)
+    a, b = dev(A), dev(B)
+    ws = gr.streamk_workspace(M, N, K)
+    ws.random_(0, 256)                                  # contents need no initialisation
+    c = gr.gemm_relu_streamk(a, b, workspace=ws)
+    got = host(c)
+    assert gr.status() == gr.OK
+    _sampled_parity(orc, A, B, got, (M, N, K))
+    # bit-identical on a second call; close to the data-parallel kernel
+    c2 = gr.gemm_relu_streamk(a, b, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16), c2.view(torch.int16))
+    ref = gr.gemm_relu(a, b)
+    torch.testing.assert_close(c.float(), ref.float(), rtol=1e-2, atol=1e-3)
+
+
+def test_streamk_falls_back_without_a_cut():
+    import torch
+    # 1024 x 2048 x 512: 32 tiles, fewer than the SMs -> plain kernel, no workspace
+    assert gr.gemm_relu_f16_streamk_workspace_bytes(1024, 2048, 512) == 0
+    A, B = inputs.make(1024, 2048, 512, seed=3)
+    a, b = dev(A), dev(B)
+    c = torch.empty((1024, 2048), dtype=torch.float16, device="cuda")
+    rc = gr.gemm_relu_f16_streamk(a.data_ptr(), b.data_ptr(), c.data_ptr(), 1024, 2048, 512,
+                                  None, 0, torch.cuda.current_stream().cuda_stream)
+    assert rc == gr.OK
+    assert torch.equal(c.view(torch.int16), gr.gemm_relu(a, b).view(torch.int16))
+
+
+# ----------------------------------------------------------------- every kernel variant
+
+KERNELS = {"one_cta_256": 1, "one_cta_128": 2, "cta_pair": 3}
+
+
+@pytest.fixture
+def forced_kernel(request):
+    gr.gemm_relu_debug_force_kernel(KERNELS[request.param])
+    yield request.param
+    gr.gemm_relu_debug_force_kernel(0)
+
+
+@pytest.mark.parametrize("forced_kernel", sorted(KERNELS), indirect=True)
+def test_each_kernel_sweep_and_workloads(orc, forced_kernel):
+    _sweep(orc, TMA_SHAPES[::3] + [(256, 256, 64), (512, 768, 192), (300, 520, 136)], gr.PATH_TMA)
+    for name in ("square1024", "square256"):
+        w = inputs.WORKLOADS[name]
+        A, B = inputs.make_workload(w)
+        assert_parity(run_fused(A, B), orc.gemm_relu_f16(A, B), abs_dot(A, B), w.K,
+                      (forced_kernel, name))
+
+
+@pytest.mark.parametrize("forced_kernel", sorted(KERNELS), indirect=True)
+def test_each_kernel_square4096_sampled(orc, forced_kernel):
+    w = inputs.WORKLOADS["square4096"]
+    A, B = inputs.make_workload(w)
+    got = run_fused(A, B)
+    _sampled_parity(orc, A, B, got, (forced_kernel, "square4096"))
+
+
+@pytest.mark.parametrize("forced_kernel", ["cta_pair"], indirect=True)
+def test_pair_integer_inputs_bit_exact(orc, forced_kernel):
+    rng = np.random.default_rng(21)
+    for (M, N, K) in [(520, 776, 64), (256, 256, 32), (1000, 264, 48)]:
+        A = rng.integers(-4, 5, (M, K)).astype(np.float16)
+        B = rng.integers(-4, 5, (K, N)).astype(np.float16)
+        assert np.array_equal(run_fused(A, B).astype(np.float64),
+                              orc.gemm_relu_f16(A, B).astype(np.float64))

@@ -40,3 +40,40 @@ def test_dropped_arrival_times_out_and_recovers(orc, kind):
     c = gr.gemm_relu_splitk(a, b, 4) if kind == "splitk" else gr.gemm_relu(a, b)
     assert gr.status() == gr.OK
     assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, kind)
+
+
+def test_streamk_dropped_arrival_times_out_and_recovers(orc):
+    M, N, K = 2048, 5120, 320
+    A, B = inputs.make(M, N, K, seed=9)
+    a, b = dev(A), dev(B)
+    gr.gemm_relu_debug_force_kernel(gr.KERNEL_ONE_CTA_256)
+    try:
+        ws = gr.streamk_workspace(M, N, K)
+        gr.gemm_relu_debug_set(1, 20_000_000)
+        gr.gemm_relu_streamk(a, b, workspace=ws)
+        assert gr.status() == gr.ERR_TIMEOUT
+        gr.gemm_relu_debug_set(0, 0)
+        c = gr.gemm_relu_streamk(a, b, workspace=ws)
+        assert gr.status() == gr.OK
+    finally:
+        gr.gemm_relu_debug_force_kernel(0)
+    rows = list(range(0, M, 97))
+    want = np.concatenate([orc.gemm_relu_f16_rows(A, B, r, 1) for r in rows])
+    assert_parity(host(c)[rows], want, abs_dot(A[rows], B), K, "streamk after timeout")
+
+
+def test_pair_kernel_dropped_arrival_times_out_and_recovers(orc):
+    M, N, K = 512, 1024, 512
+    A, B = inputs.make(M, N, K, seed=10)
+    a, b = dev(A), dev(B)
+    gr.gemm_relu_debug_force_kernel(gr.KERNEL_PAIR)
+    try:
+        gr.gemm_relu_debug_set(1, 20_000_000)
+        gr.gemm_relu(a, b)
+        assert gr.status() == gr.ERR_TIMEOUT
+        gr.gemm_relu_debug_set(0, 0)
+        c = gr.gemm_relu(a, b)
+        assert gr.status() == gr.OK
+        assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, "pair after timeout")
+    finally:
+        gr.gemm_relu_debug_force_kernel(0)

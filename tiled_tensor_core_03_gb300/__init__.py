@@ -52,6 +52,10 @@ def lib():
         L.gemm_relu_f16_splitk_workspace_bytes.restype = sz
         L.gemm_relu_f16_splitk.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
         L.gemm_relu_f16_splitk.restype = i32
+        L.gemm_relu_f16_streamk_workspace_bytes.argtypes = [i64, i64, i64]
+        L.gemm_relu_f16_streamk_workspace_bytes.restype = sz
+        L.gemm_relu_f16_streamk.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        L.gemm_relu_f16_streamk.restype = i32
         L.gemm_relu_f16_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
         L.gemm_relu_f16_splitk_noalloc.restype = i32
         L.gemm_relu_status.argtypes = [vp]
@@ -63,6 +67,8 @@ def lib():
         L.gemm_relu_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
                                            ctypes.POINTER(i64)]
         L.gemm_relu_tile_coord.restype = i32
+        L.gemm_relu_debug_force_kernel.argtypes = [i32]
+        L.gemm_relu_debug_force_kernel.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
         L.gemm_relu_debug_set.restype = i32
         _lib = L
@@ -74,6 +80,14 @@ def lib():
 
 def gemm_relu_f16(A, B, C, M, N, K, stream=None):
     return lib().gemm_relu_f16(A, B, C, M, N, K, stream)
+
+
+def gemm_relu_f16_streamk_workspace_bytes(M, N, K):
+    return lib().gemm_relu_f16_streamk_workspace_bytes(M, N, K)
+
+
+def gemm_relu_f16_streamk(A, B, C, M, N, K, workspace, workspace_bytes, stream=None):
+    return lib().gemm_relu_f16_streamk(A, B, C, M, N, K, workspace, workspace_bytes, stream)
 
 
 def gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k):
@@ -113,6 +127,13 @@ def gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel):
     if rc != 0:
         raise ValueError("tile out of range")
     return mb.value, nb.value
+
+
+KERNEL_AUTO, KERNEL_ONE_CTA_256, KERNEL_ONE_CTA_128, KERNEL_PAIR = 0, 1, 2, 3
+
+
+def gemm_relu_debug_force_kernel(which):
+    return lib().gemm_relu_debug_force_kernel(int(which))
 
 
 def gemm_relu_debug_set(drop_arrive=0, wait_limit_ns=0):
@@ -160,6 +181,30 @@ def gemm_relu(a, b, out=None, stream=None):
     rc = gemm_relu_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, _stream_ptr(stream))
     if rc != OK:
         raise GemmReluError(rc, "gemm_relu_f16")
+    return c
+
+
+def streamk_workspace(M, N, K, device=None):
+    """A device workspace sized for gemm_relu_streamk (uint8 tensor, may be tiny)."""
+    import torch
+    n = gemm_relu_f16_streamk_workspace_bytes(M, N, K)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def gemm_relu_streamk(a, b, out=None, workspace=None, stream=None):
+    """Same result as gemm_relu (up to fp32 summation order in the tiles the
+    schedule cuts), with a stream-K schedule for the partial last wave."""
+    _check_operands(a, b)
+    c = _out(a, b, out)
+    M, K = a.shape
+    N = b.shape[1]
+    if workspace is None:
+        workspace = streamk_workspace(M, N, K, a.device)
+    rc = gemm_relu_f16_streamk(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_ptr(stream))
+    if rc != OK:
+        raise GemmReluError(rc, "gemm_relu_f16_streamk")
     return c
 
 

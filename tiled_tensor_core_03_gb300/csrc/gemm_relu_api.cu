@@ -18,6 +18,7 @@
 #include "gemm_relu.h"
 #include "gemm_relu_kernels.cuh"
 #include "gemm_relu_splitk.cuh"
+#include "gemm_relu_2sm.cuh"
 
 namespace {
 
@@ -37,6 +38,13 @@ constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;
 // ---------------------------------------------------------------- test hooks
 std::atomic<int> g_drop_arrive{0};
 std::atomic<int64_t> g_wait_limit_ns{0};
+std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 128, 3 CTA pair
+std::atomic<uint32_t> g_epoch{0};
+
+uint32_t next_epoch() {
+    uint32_t e = ++g_epoch;
+    return e ? e : ++g_epoch;
+}
 
 uint64_t wait_limit_ns() {
     const int64_t v = g_wait_limit_ns.load();
@@ -48,8 +56,9 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
-    bool attr_fused[2] = {false, false};
+    bool attr_fused[4] = {false, false, false, false};
     bool attr_split[4] = {false, false, false, false};
+    bool attr_pair = false;
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -157,10 +166,116 @@ int zero_fill(void *C, int64_t M, int64_t N, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------- fused launch
+#ifndef GEMMRELU_FUSED_BN
+#define GEMMRELU_FUSED_BN 0       // 0: choose per shape; 128 or 256: force
+#endif
+
+// Tile width of the fused kernel: 256 unless 128-wide tiles fill the SMs in
+// fewer weighted waves.  Measured on GB300, a 128-wide tile costs about 0.7 of
+// a 256-wide one (its MMAs are bound by shared-memory bandwidth), so 128 only
+// wins when it turns a partial wave into a full one, as at 1024^3.
+int fused_bn(int64_t M, int64_t N, int sms) {
+    if (GEMMRELU_FUSED_BN == 128 || GEMMRELU_FUSED_BN == 256)
+        return GEMMRELU_FUSED_BN;
+    if (g_force_kernel.load() == 1)
+        return 256;
+    if (g_force_kernel.load() == 2)
+        return 128;
+    const int64_t mt = (M + 127) / 128;
+    const int64_t w256 = (mt * ((N + 255) / 256) + sms - 1) / sms;
+    const int64_t w128 = (mt * ((N + 127) / 128) + sms - 1) / sms;
+    return (double)w128 * 0.7 < (double)w256 ? 128 : 256;
+}
+
+template <bool kTma, int kBN>
+int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensorMap &mC,
+                    const gemmrelu::fused::Params &p, cudaStream_t stream, DeviceState *ds,
+                    bool &attr_done) {
+    namespace F = gemmrelu::fused;
+    auto kern = F::gemm_relu_fused_kernel<kTma, kBN>;
+    constexpr uint32_t smem = F::Tile<kBN>::kSmemBytes;
+    if (!ensure_smem_attr(attr_done, kern, smem))
+        return GEMMRELU_ERR_LAUNCH;
+    const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
+    if (p.dp_tiles == p.num_tiles) {
+        kern<<<(unsigned)grid, F::Roles<kTma>::kThreads, smem, stream>>>(mA, mB, mC, p);
+        return launch_status(cudaGetLastError());
+    }
+    // Stream-K: CTAs wait on flags raised by their neighbours, so all of them
+    // must be resident at once -- a cooperative launch guarantees that (or
+    // fails).
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(F::Roles<kTma>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p));
+}
+
+// ---------------------------------------------------------------- CTA-pair launch
+// 256 x 256 tiles on CTA pairs (2-SM MMA).  TMA path only.
+int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                cudaStream_t stream, DeviceState *ds) {
+    namespace P = gemmrelu::pair;
+    namespace F = gemmrelu::fused;
+    P::Params p{};
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.num_kb = (int)((K + P::BK - 1) / P::BK);
+    p.m_tiles = (M + P::BMP - 1) / P::BMP;
+    p.n_tiles = (N + P::BNP - 1) / P::BNP;
+    p.num_tiles = p.m_tiles * p.n_tiles;
+    p.panel = kPanel / 2;                       // same 1024-row panels as the single-CTA kernel
+    p.drop_arrive = g_drop_arrive.load();
+    p.wait_limit_ns = wait_limit_ns();
+    CUtensorMap mA, mB, mC;
+    if (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
+        !make_map(&mC, C, M, N, 64, 32))
+        return GEMMRELU_ERR_LAUNCH;
+    if (!ensure_smem_attr(ds->attr_pair, P::gemm_relu_pair_kernel, P::kSmemBytes))
+        return GEMMRELU_ERR_LAUNCH;
+    const int64_t pairs = std::min<int64_t>(p.num_tiles, ds->sms / 2);
+    P::gemm_relu_pair_kernel<<<(unsigned)(2 * pairs), P::kThreads, P::kSmemBytes, stream>>>(
+        mA, mB, mC, p);
+    return launch_status(cudaGetLastError());
+}
+
+// Whether gemm_relu_f16 runs the CTA-pair kernel: TMA operands, at least one
+// full 256 x 256 tile, and no more weighted waves than the single-CTA choice
+// (a 256 x 256 pair tile does the work of two 128 x 256 tiles on two SMs).
+bool use_pair(int64_t M, int64_t N, int sms, int path) {
+    const int force = g_force_kernel.load();
+    if (force == 3)
+        return path == 1;
+    if (force == 1 || force == 2)
+        return false;
+    if (path != 1 || M < 256 || N < 256 || sms < 2)
+        return false;
+    const int64_t pair_waves = ((M + 255) / 256 * ((N + 255) / 256) + sms / 2 - 1) / (sms / 2);
+    const int64_t one_waves = ((M + 127) / 128 * ((N + 255) / 256) + sms - 1) / sms;
+    return pair_waves <= one_waves;
+}
+
+// Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
+struct StreamK {
+    int64_t dp_tiles = -1;     // -1: plain data-parallel launch
+    float *part = nullptr;
+    uint32_t *flags = nullptr;
+    uint32_t epoch = 0;
+};
+
 int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                 cudaStream_t stream, DeviceState *ds) {
+                 cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
     namespace F = gemmrelu::fused;
     const int path = fused_path(A, B, C, M, N, K);
+    if (sk.dp_tiles < 0 && use_pair(M, N, ds->sms, path))
+        return launch_pair(A, B, C, M, N, K, stream, ds);
     F::Params p{};
     p.A = static_cast<const uint16_t *>(A);
     p.B = static_cast<const uint16_t *>(B);
@@ -169,33 +284,54 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     p.N = (int)N;
     p.K = (int)K;
     p.num_kb = (int)((K + F::BK - 1) / F::BK);
+    const int bn = fused_bn(M, N, ds->sms);
     p.m_tiles = (M + F::BM - 1) / F::BM;
-    p.n_tiles = (N + F::BN - 1) / F::BN;
+    p.n_tiles = (N + bn - 1) / bn;
     p.num_tiles = p.m_tiles * p.n_tiles;
     p.panel = kPanel;
     p.drop_arrive = g_drop_arrive.load();
     p.wait_limit_ns = wait_limit_ns();
-    const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
-
+    p.dp_tiles = sk.dp_tiles >= 0 ? sk.dp_tiles : p.num_tiles;
+    p.sk_part = sk.part;
+    p.sk_flags = sk.flags;
+    p.epoch = sk.epoch;
     CUtensorMap mA, mB, mC;
     std::memset(&mA, 0, sizeof(mA));
     std::memset(&mB, 0, sizeof(mB));
     std::memset(&mC, 0, sizeof(mC));
-    if (path == 1) {
-        if (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
-            !make_map(&mC, C, M, N, 64, 32))
-            return GEMMRELU_ERR_LAUNCH;
-        auto kern = F::gemm_relu_fused_kernel<true>;
-        if (!ensure_smem_attr(ds->attr_fused[0], kern, F::kSmemBytes))
-            return GEMMRELU_ERR_LAUNCH;
-        kern<<<(unsigned)grid, F::Roles<true>::kThreads, F::kSmemBytes, stream>>>(mA, mB, mC, p);
-    } else {
-        auto kern = F::gemm_relu_fused_kernel<false>;
-        if (!ensure_smem_attr(ds->attr_fused[1], kern, F::kSmemBytes))
-            return GEMMRELU_ERR_LAUNCH;
-        kern<<<(unsigned)grid, F::Roles<false>::kThreads, F::kSmemBytes, stream>>>(mA, mB, mC, p);
+    if (path == 1 &&
+        (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
+         !make_map(&mC, C, M, N, 64, 32)))
+        return GEMMRELU_ERR_LAUNCH;
+    if (bn == 256) {
+        if (path == 1)
+            return launch_fused_bn<true, 256>(mA, mB, mC, p, stream, ds, ds->attr_fused[0]);
+        return launch_fused_bn<false, 256>(mA, mB, mC, p, stream, ds, ds->attr_fused[1]);
     }
-    return launch_status(cudaGetLastError());
+    if (path == 1)
+        return launch_fused_bn<true, 128>(mA, mB, mC, p, stream, ds, ds->attr_fused[2]);
+    return launch_fused_bn<false, 128>(mA, mB, mC, p, stream, ds, ds->attr_fused[3]);
+}
+
+// ---------------------------------------------------------------- stream-K plan
+// For 128 x 256 tiles on a TMA-able problem: when the tiles do not fill a
+// whole number of waves, all but the last full wave run data-parallel and
+// the rest is spread evenly over the grid.  Returns the number of
+// data-parallel tiles, or -1 when stream-K does not apply.
+int64_t streamk_dp_tiles(int64_t M, int64_t N, int sms, int64_t *grid_out) {
+    if (fused_bn(M, N, sms) != 256 || use_pair(M, N, sms, 1))
+        return -1;
+    const int64_t T = ((M + 127) / 128) * ((N + 255) / 256);
+    const int64_t G = std::min<int64_t>(T, sms);
+    if (grid_out)
+        *grid_out = G;
+    if (T <= G || T % G == 0)
+        return -1;
+    return (T / G - 1) * G;
+}
+
+size_t streamk_bytes(int64_t grid) {
+    return (size_t)grid * 256 * 128 * 4 + (size_t)grid * 4 * 4;
 }
 
 // ---------------------------------------------------------------- split-K
@@ -340,6 +476,47 @@ int gemm_relu_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, i
     return launch_fused(A, B, C, M, N, K, s, ds);
 }
 
+size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return 0;
+    DeviceState *ds = nullptr;
+    if (current_device_state(&ds) != GEMMRELU_OK)
+        return 0;
+    int64_t grid = 0;
+    if (streamk_dp_tiles(M, N, ds->sms, &grid) < 0)
+        return 0;
+    return streamk_bytes(grid);
+}
+
+int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_args(A, B, C, M, N, K);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    if (M == 0 || N == 0)
+        return GEMMRELU_OK;
+    DeviceState *ds = nullptr;
+    rc = current_device_state(&ds);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)
+        return zero_fill(C, M, N, s);
+    int64_t grid = 0;
+    const int64_t dp = streamk_dp_tiles(M, N, ds->sms, &grid);
+    if (dp < 0 || fused_path(A, B, C, M, N, K) != 1)
+        return launch_fused(A, B, C, M, N, K, s, ds);
+    if (!workspace || workspace_bytes < streamk_bytes(grid) || !aligned(workspace, 16))
+        return GEMMRELU_ERR_WORKSPACE;
+    StreamK sk;
+    sk.dp_tiles = dp;
+    sk.part = static_cast<float *>(workspace);
+    sk.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
+                                            (size_t)grid * 256 * 128 * 4);
+    sk.epoch = next_epoch();
+    return launch_fused(A, B, C, M, N, K, s, ds, sk);
+}
+
 size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int split_k) {
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || split_k < 1)
         return 0;
@@ -446,6 +623,13 @@ int gemm_relu_tile_coord(int64_t tile, int64_t m_tiles, int64_t n_tiles, int pan
     *m_blk = mb;
     *n_blk = nb;
     return 0;
+}
+
+int gemm_relu_debug_force_kernel(int which) {
+    if (which < 0 || which > 3)
+        return GEMMRELU_ERR_INVALID_ARG;
+    g_force_kernel.store(which);
+    return GEMMRELU_OK;
 }
 
 int gemm_relu_debug_set(int drop_arrive, int64_t wait_limit_ns_arg) {

@@ -50,6 +50,7 @@ enum WaitSite : unsigned {
     kSiteMmaFull = 3,
     kSiteEpiAccFull = 4,
     kSiteDrain = 5,
+    kSitePieceFlag = 6,
 };
 
 __device__ __forceinline__ void record_timeout(volatile uint32_t *abort_flag, unsigned where) {
@@ -188,28 +189,32 @@ __device__ __forceinline__ void tmem_ld_x16_sync(uint32_t taddr, uint32_t (&r)[1
 namespace fused {
 
 constexpr int BM = 128;            // UMMA M: TMEM lanes = output rows
-constexpr int BN = 256;            // UMMA N: TMEM columns per accumulator
 constexpr int BK = 64;             // one 128-byte swizzle row of fp16
 constexpr int UK = 16;             // K of one tcgen05.mma kind::f16
-constexpr int kStages = 4;
 constexpr uint32_t kATile = BM * BK * 2;    // 16 KB, K-major, 128 rows x 128 B
 constexpr uint32_t kBSlab = BK * 64 * 2;    // 8 KB: 64 k-rows x 64 n (128 B)
-constexpr uint32_t kBTile = BK * BN * 2;    // 32 KB = 4 slabs, MN-major
 constexpr uint32_t kEpiBuf = 32 * 128;      // 32 rows x 64 fp16, swizzled
 constexpr int kEpiWarps = 4;
-constexpr uint32_t kTmemCols = 2 * BN;      // double-buffered accumulator
 
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kATile;
-constexpr uint32_t kOffEpi = kOffB + kStages * kBTile;
-constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
-constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
-
-// A: K-major (bit 15 = 0); B: N-major (bit 16 = 1); M = 128, N = 256.
-constexpr uint32_t kIdesc = make_idesc_f16_f32(BM, BN, 0, 1);
+// Per tile width BN (UMMA N = TMEM columns per accumulator): 256 or 128.
+// The ring gets as many stages as fit beside 32 KB of epilogue staging.
+template <int kBN>
+struct Tile {
+    static constexpr int BN = kBN;
+    static constexpr uint32_t kBTile = BK * BN * 2;          // BN / 64 slabs, MN-major
+    static constexpr int kStages = kBN >= 256 ? 4 : 6;
+    static constexpr uint32_t kTmemCols = 2 * BN;            // double-buffered accumulator
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kOffA + kStages * kATile;
+    static constexpr uint32_t kOffEpi = kOffB + kStages * kBTile;
+    static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
+    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemUsed = kOffMisc + 16;
+    static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+    // A: K-major (bit 15 = 0); B: N-major (bit 16 = 1); M = 128, N = BN.
+    static constexpr uint32_t kIdesc = make_idesc_f16_f32(BM, BN, 0, 1);
+};
 
 struct Params {
     const uint16_t *A;
@@ -221,7 +226,97 @@ struct Params {
     int panel;
     int drop_arrive;
     uint64_t wait_limit_ns;
+    // Stream-K schedule ("TileLang tutorial", chapter "Persistent kernel":
+    // split-K / stream-K remove the partial last wave).  Tiles [0, dp_tiles)
+    // run data-parallel: CTA c takes tiles c, c + G, ...  The k blocks of the
+    // remaining tiles are laid end to end and cut into G equal contiguous
+    // ranges, one per CTA, so every CTA gets the same amount of MMA work.  A
+    // tile cut between CTA c (its first k blocks, at the end of c's range) and
+    // CTA c + 1 (its last k blocks, at the start of c + 1's range) is summed
+    // through sk_part: c + 1 stores its fp32 piece and raises sk_flags[c + 1],
+    // c adds it to its own piece before the ReLU epilogue.  dp_tiles equal to
+    // num_tiles means no stream-K part.
+    int64_t dp_tiles;
+    float *sk_part;        // [G][BN][BM] fp32 pieces, column-major per slot
+    uint32_t *sk_flags;    // [G][4]: one flag per epilogue warp (32 rows)
+    uint32_t epoch;        // nonzero, distinct per call
 };
+
+enum ItemKind : int { kItemFull = 0, kItemPieceOut = 1, kItemPieceIn = 2 };
+
+// Number of work items of CTA c (data-parallel tiles, then stream-K pieces).
+__device__ __forceinline__ int64_t num_items(const Params &p, int64_t c, int64_t G) {
+    const int64_t ndp = c < p.dp_tiles ? (p.dp_tiles - 1 - c) / G + 1 : 0;
+    const int64_t W = (p.num_tiles - p.dp_tiles) * p.num_kb;
+    const int64_t s = c * W / G, e = (c + 1) * W / G;
+    if (e <= s)
+        return ndp;
+    return ndp + (e - 1) / p.num_kb - s / p.num_kb + 1;
+}
+
+// Item i of CTA c: tile id, k-block range [kb0, kb1) and kind.  A piece that
+// starts inside its tile is the tile's k tail (kItemPieceOut, stored for the
+// previous CTA); one that stops inside is the k head (kItemPieceIn, adds the
+// next CTA's stored tail).  Each range is at least one tile long, so a piece
+// is never both.
+__device__ __forceinline__ void item_at(const Params &p, int64_t c, int64_t G, int64_t i,
+                                        int64_t &tile, int &kb0, int &kb1, int &kind) {
+    const int64_t ndp = c < p.dp_tiles ? (p.dp_tiles - 1 - c) / G + 1 : 0;
+    if (i < ndp) {
+        tile = c + i * G;
+        kb0 = 0;
+        kb1 = p.num_kb;
+        kind = kItemFull;
+        return;
+    }
+    const int64_t W = (p.num_tiles - p.dp_tiles) * p.num_kb;
+    const int64_t s = c * W / G, e = (c + 1) * W / G;
+    const int64_t t = s / p.num_kb + (i - ndp);
+    const int64_t lo = t * p.num_kb;
+    kb0 = (int)((s > lo ? s : lo) - lo);
+    kb1 = (int)((e < lo + p.num_kb ? e : lo + p.num_kb) - lo);
+    tile = p.dp_tiles + t;
+    kind = kb0 > 0 ? kItemPieceOut : (kb1 < p.num_kb ? kItemPieceIn : kItemFull);
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All lanes wait until *f == v (a stream-K piece published by another CTA);
+// bounded like every other wait.
+__device__ __forceinline__ bool wait_flag(const uint32_t *f, uint32_t v, uint64_t limit_ns,
+                                          volatile uint32_t *abort_flag) {
+    if (ld_acquire_gpu(f) == v)
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(f) == v)
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout(abort_flag, kSitePieceFlag);
+            return false;
+        }
+    }
+}
+
+// r[j] += the 32 fp32 columns at TMEM address taddr (this lane's row).
+__device__ __forceinline__ void add_tmem(uint32_t (&r)[32], uint32_t taddr) {
+    uint32_t o[32];
+    tmem_ld_x32_sync(taddr, o);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(o[j]));
+}
 
 template <bool kTma>
 struct Roles {
@@ -231,12 +326,18 @@ struct Roles {
     static constexpr int kThreads = 32 * (kLoadWarps + 1 + kEpiWarps);
 };
 
-template <bool kTma>
+template <bool kTma, int kBN>
 __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     gemm_relu_fused_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const Params p) {
     using R = Roles<kTma>;
+    using T = Tile<kBN>;
+    constexpr int BN = T::BN;
+    constexpr int kStages = T::kStages;
+    constexpr uint32_t kBTile = T::kBTile, kTmemCols = T::kTmemCols, kIdesc = T::kIdesc;
+    constexpr uint32_t kOffA = T::kOffA, kOffB = T::kOffB, kOffEpi = T::kOffEpi;
+    constexpr uint32_t kOffBar = T::kOffBar, kOffMisc = T::kOffMisc;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -287,18 +388,20 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             if (lane == 0) {
                 uint32_t stage = 0, phase = 0, issued = 0, parity = 0;
                 bool ok = true;
-                for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                    int64_t mb, nb;
+                const int64_t items = num_items(p, blockIdx.x, gridDim.x);
+                for (int64_t it = 0; ok && it < items; ++it) {
+                    int64_t t, mb, nb;
+                    int kb0, kb1, kind;
+                    item_at(p, blockIdx.x, gridDim.x, it, t, kb0, kb1, kind);
                     tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
                     const int m0 = (int)(mb * BM), n0 = (int)(nb * BN);
-                    for (int kb = 0; kb < p.num_kb; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb) {
                         if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
                                           kSiteProducerEmpty)) {
                             ok = false;
                             break;
                         }
-                        const bool drop =
-                            p.drop_arrive && blockIdx.x == 0 && t == blockIdx.x && kb == 0;
+                        const bool drop = p.drop_arrive && blockIdx.x == 0 && it == 0 && kb == kb0;
                         if (!drop) {
                             const uint32_t fb = full_bar(stage);
                             mbar_arrive_expect_tx(fb, kATile + kBTile);
@@ -327,11 +430,14 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const int tid = threadIdx.x;  // 0 .. 127
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                int64_t mb, nb;
+            const int64_t items = num_items(p, blockIdx.x, gridDim.x);
+            for (int64_t it = 0; ok && it < items; ++it) {
+                int64_t t, mb, nb;
+                int kb0, kb1, kind;
+                item_at(p, blockIdx.x, gridDim.x, it, t, kb0, kb1, kind);
                 tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
                 const int64_t m0 = mb * BM, n0 = nb * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
                                       kSiteProducerEmpty)) {
                         ok = false;
@@ -349,7 +455,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     }
                     const uint32_t bdst = base + kOffB + stage * kBTile;
                     for (int c = tid; c < BK * (BN / 8); c += 128) {
-                        const int j = c & 7, s = (c >> 3) & 3, r = c >> 5;
+                        const int j = c & 7, s = (c >> 3) % (BN / 64), r = (c >> 3) / (BN / 64);
                         const int64_t gk = k0 + r;
                         uint4 v = make_uint4(0u, 0u, 0u, 0u);
                         if (gk < p.K)
@@ -357,8 +463,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                         st_shared_v4(bdst + s * kBSlab + sw128_offset(r, j), v.x, v.y, v.z, v.w);
                     }
                     fence_proxy_async_smem();
-                    const bool drop =
-                        p.drop_arrive && blockIdx.x == 0 && t == blockIdx.x && kb == 0;
+                    const bool drop = p.drop_arrive && blockIdx.x == 0 && it == 0 && kb == kb0;
                     if (!drop)
                         mbar_arrive(full_bar(stage));
                     if (++stage == kStages) {
@@ -373,15 +478,18 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            int64_t i = 0;
-            for (int64_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++i) {
+            const int64_t items = num_items(p, blockIdx.x, gridDim.x);
+            for (int64_t i = 0; ok && i < items; ++i) {
+                int64_t t;
+                int kb0, kb1, kind;
+                item_at(p, blockIdx.x, gridDim.x, i, t, kb0, kb1, kind);
                 const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
                 if (!wait_bounded(acce_bar(buf), use ^ 1u, p.wait_limit_ns, abort_flag,
                                   kSiteMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + buf * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
                                       kSiteMmaFull)) {
                         ok = false;
@@ -399,7 +507,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                         // further; 64-wide N slabs kBSlab apart (LBO), 8-row
                         // k groups 1024 B apart (SBO).
                         const uint64_t bdesc = make_sdesc_sw128(b + kk * (UK * 128), kBSlab, 1024);
-                        umma_f16(d, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16(d, adesc, bdesc, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == kStages) {
@@ -422,14 +530,78 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * 2u * kEpiBuf;
         uint32_t nstores = 0;
-        int64_t i = 0;
-        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+        const int64_t items = num_items(p, blockIdx.x, gridDim.x);
+        // Stream-K: when the last item is a k head piece, the next CTA's
+        // published k tail is copied into the other TMEM accumulator buffer
+        // once the item before the k head has been read (that buffer is not
+        // used again), while the MMA works on the k head; the k head's
+        // epilogue then adds the two buffers.  The MMA never waits for it, and
+        // this CTA has published its own k tail (its first stream-K item)
+        // before it waits for its neighbour's, so waits cannot chain.
+        int64_t last_t = 0;
+        int last_kb0 = 0, last_kb1 = 0, last_kind = kItemFull;
+        if (items > 0)
+            item_at(p, blockIdx.x, gridDim.x, items - 1, last_t, last_kb0, last_kb1, last_kind);
+        const bool preload = last_kind == kItemPieceIn && items >= 2;
+        const uint32_t partner_buf = tmem_base + lane_base + (uint32_t)((items - 2) & 1) * BN;
+        auto preload_piece = [&]() -> bool {
+            uint32_t *flag = p.sk_flags + (blockIdx.x + 1) * 4 + q;
+            const bool got = wait_flag(flag, p.epoch, p.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got))
+                return false;
+            const float *src = p.sk_part + (size_t)(blockIdx.x + 1) * BN * BM + 32 * q + lane;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __float_as_uint(__ldcg(src + (size_t)(32 * c + j) * BM));
+                tmem_st_x32(partner_buf + 32 * c, v);
+            }
+            tmem_st_wait();
+            __syncwarp();
+            if (lane == 0)
+                *flag = 0u;  // consumed: no later call can mistake it for its own
+            return true;
+        };
+        bool alive = true;
+        for (int64_t i = 0; alive && i < items; ++i) {
+            int64_t t;
+            int kb0, kb1, kind;
+            item_at(p, blockIdx.x, gridDim.x, i, t, kb0, kb1, kind);
             const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
             const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
                                          kSiteEpiAccFull);
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after_sync();
+            const uint32_t acc = tmem_base + lane_base + buf * BN;
+            const bool preload_next = preload && i == items - 2;
+            if (kind == kItemPieceOut) {
+                // k tail of a tile cut with the previous CTA: publish the raw
+                // fp32 piece in this CTA's slot, [column][row] so that each
+                // warp store covers 32 consecutive rows (128 bytes).
+                float *dst = p.sk_part + (size_t)blockIdx.x * BN * BM + 32 * q + lane;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_x32_sync(acc + 32 * c, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(dst + (size_t)(32 * c + j) * BM, __uint_as_float(r[j]));
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    st_release_gpu(p.sk_flags + blockIdx.x * 4 + q, p.epoch);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acce_bar(buf));
+                if (preload_next && !preload_piece())
+                    break;
+                continue;
+            }
             int64_t mb, nb;
             tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
             const int64_t row0 = mb * BM + 32 * q;
@@ -440,12 +612,16 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 if (row0 >= p.M || col0 >= p.N)
                     continue;  // warp-uniform: nothing of this chunk is in C
                 uint32_t r[32], h[32];
-                const uint32_t taddr = tmem_base + lane_base + buf * BN + 64 * c;
+                const uint32_t taddr = acc + 64 * c;
                 tmem_ld_x32_sync(taddr, r);
+                if (kind == kItemPieceIn)
+                    add_tmem(r, partner_buf + 64 * c);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
                 tmem_ld_x32_sync(taddr + 32, r);
+                if (kind == kItemPieceIn)
+                    add_tmem(r, partner_buf + 64 * c + 32);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
@@ -498,6 +674,8 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acce_bar(buf));
+            if (preload_next && !preload_piece())
+                break;
         }
         if constexpr (kTma) {
             if (lane == 0)
