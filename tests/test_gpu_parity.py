@@ -239,6 +239,8 @@ def test_error_growth_is_smooth(orc):
 
 # ----------------------------------------------------------------- stream-K
 
+KERNELS = {"one_cta_256": 1, "one_cta_128": 2, "cta_pair": 3}
+
 
 def _sampled_parity(orc, A, B, got, what, seed=7):
     M, K = A.shape
@@ -257,16 +259,16 @@ def _sampled_parity(orc, A, B, got, what, seed=7):
 STREAMK_SHAPES = [(4096, 4096, 4096), (2048, 5120, 320), (2000, 4104, 776), (3000, 4352, 64)]
 
 
-@pytest.fixture
-def one_cta():
-    """The single-CTA kernel (where the stream-K schedule lives)."""
-    gr.gemm_relu_debug_force_kernel(1)
-    yield
+@pytest.fixture(params=["one_cta_256", "cta_pair"])
+def sk_kernel(request):
+    """Stream-K runs on the single-CTA kernel and on CTA pairs."""
+    gr.gemm_relu_debug_force_kernel(KERNELS[request.param])
+    yield request.param
     gr.gemm_relu_debug_force_kernel(0)
 
 
 @pytest.mark.parametrize("M,N,K", STREAMK_SHAPES)
-def test_streamk_parity(orc, one_cta, M, N, K):
+def test_streamk_parity(orc, sk_kernel, M, N, K):
     import torch
     assert gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K) > 0, "shape has no stream-K part"
     A, B = inputs.make(M, N, K, "normal", True, seed=M + N + K)
@@ -299,9 +301,6 @@ def test_streamk_falls_back_without_a_cut():
 
 
 # ----------------------------------------------------------------- every kernel variant
-
-KERNELS = {"one_cta_256": 1, "one_cta_128": 2, "cta_pair": 3}
-
 
 @pytest.fixture
 def forced_kernel(request):

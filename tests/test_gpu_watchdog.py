@@ -42,11 +42,12 @@ def test_dropped_arrival_times_out_and_recovers(orc, kind):
     assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, kind)
 
 
-def test_streamk_dropped_arrival_times_out_and_recovers(orc):
+@pytest.mark.parametrize("kernel", [1, 3])
+def test_streamk_dropped_arrival_times_out_and_recovers(orc, kernel):
     M, N, K = 2048, 5120, 320
     A, B = inputs.make(M, N, K, seed=9)
     a, b = dev(A), dev(B)
-    gr.gemm_relu_debug_force_kernel(gr.KERNEL_ONE_CTA_256)
+    gr.gemm_relu_debug_force_kernel(kernel)
     try:
         ws = gr.streamk_workspace(M, N, K)
         gr.gemm_relu_debug_set(1, 20_000_000)

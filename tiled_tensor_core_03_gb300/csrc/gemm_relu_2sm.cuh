@@ -40,6 +40,12 @@ using fused::kATile;      // 128 rows x 64 k of A per CTA (16 KB)
 using fused::kBSlab;      // 64 k x 64 n of B (8 KB)
 using fused::kEpiBuf;
 using fused::kEpiWarps;
+using fused::SkShape;
+using fused::sk_num_items;
+using fused::sk_item_at;
+using fused::kItemFull;
+using fused::kItemPieceIn;
+using fused::kItemPieceOut;
 
 constexpr int BMP = 256;                        // tile rows (both CTAs)
 constexpr int BNP = 256;                        // tile columns (UMMA N)
@@ -68,6 +74,14 @@ struct Params {
     int panel;
     int drop_arrive;
     uint64_t wait_limit_ns;
+    // Stream-K over pairs, as in the single-CTA kernel: tiles [0, dp_tiles)
+    // data-parallel, the k blocks of the rest cut into one range per pair.
+    // CTA b of a pair cut with the next pair passes its 128 rows of the
+    // tile's k tail through sk_part[b] / sk_flags[b][warp] to CTA b - 2.
+    int64_t dp_tiles;
+    float *sk_part;        // [2 * pairs][BNP][128] fp32
+    uint32_t *sk_flags;    // [2 * pairs][4]
+    uint32_t epoch;
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -94,6 +108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int64_t pair_id = blockIdx.x >> 1;
     const int64_t num_pairs = gridDim.x >> 1;
+    const SkShape sk{p.num_tiles, p.dp_tiles, p.num_kb};
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
@@ -129,18 +144,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0, parity = 0;
             bool ok = true;
-            for (int64_t t = pair_id; ok && t < p.num_tiles; t += num_pairs) {
-                int64_t mb, nb;
+            const int64_t items = sk_num_items(sk, pair_id, num_pairs);
+            for (int64_t it = 0; ok && it < items; ++it) {
+                int64_t t, mb, nb;
+                int kb0, kb1, kind;
+                sk_item_at(sk, pair_id, num_pairs, it, t, kb0, kb1, kind);
                 tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
                 const int m0 = (int)(mb * BMP) + 128 * (int)rank;
                 const int n0 = (int)(nb * BNP) + kBHalf * (int)rank;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
                                       kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    const bool drop = p.drop_arrive && blockIdx.x == 0 && t == pair_id && kb == 0;
+                    const bool drop = p.drop_arrive && blockIdx.x == 0 && it == 0 && kb == kb0;
                     if (!drop) {
                         const uint32_t fb = mapa_shared(full_bar(stage), 0);
                         if (leader)
@@ -171,15 +189,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (leader && lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            int64_t i = 0;
-            for (int64_t t = pair_id; ok && t < p.num_tiles; t += num_pairs, ++i) {
+            const int64_t items = sk_num_items(sk, pair_id, num_pairs);
+            for (int64_t i = 0; ok && i < items; ++i) {
+                int64_t t;
+                int kb0, kb1, kind;
+                sk_item_at(sk, pair_id, num_pairs, i, t, kb0, kb1, kind);
                 const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
                 if (!wait_bounded(acce_bar(buf), use ^ 1u, p.wait_limit_ns, abort_flag,
                                   kSiteMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_base + buf * BNP;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
                                       kSiteMmaFull)) {
                         ok = false;
@@ -192,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < BK / UK; ++kk) {
                         const uint64_t adesc = make_sdesc_sw128(a + kk * (UK * 2), 16, 1024);
                         const uint64_t bdesc = make_sdesc_sw128(b + kk * (UK * 128), kBSlab, 1024);
-                        umma_f16_pair(d, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_f16_pair(d, adesc, bdesc, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit_pair(empty_bar(stage), 0x3);   // both CTAs may refill
                     if (++stage == (uint32_t)kStages) {
@@ -217,14 +238,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * 2u * kEpiBuf;
         uint32_t nstores = 0;
-        int64_t i = 0;
-        for (int64_t t = pair_id; t < p.num_tiles; t += num_pairs, ++i) {
+        const int64_t items = sk_num_items(sk, pair_id, num_pairs);
+        const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
+        // Stream-K k head: pre-load the next pair's published k tail (this
+        // CTA's rows) into the spare TMEM buffer once the item before it has
+        // been read; the k head's epilogue adds the two buffers.  This CTA has
+        // published its own k tail (its pair's first stream-K item) by then.
+        int64_t last_t = 0;
+        int last_kb0 = 0, last_kb1 = 0, last_kind = kItemFull;
+        if (items > 0)
+            sk_item_at(sk, pair_id, num_pairs, items - 1, last_t, last_kb0, last_kb1, last_kind);
+        const bool preload = last_kind == kItemPieceIn && items >= 2;
+        const uint32_t partner_buf = tmem_base + lane_base + (uint32_t)((items - 2) & 1) * BNP;
+        auto preload_piece = [&]() -> bool {
+            uint32_t *flag = p.sk_flags + (blockIdx.x + 2) * 4 + q;
+            const bool got = fused::wait_flag(flag, p.epoch, p.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got))
+                return false;
+            const float *src = p.sk_part + (size_t)(blockIdx.x + 2) * BNP * 128 + 32 * q + lane;
+#pragma unroll 1
+            for (int c = 0; c < BNP / 32; ++c) {
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    v[j] = __float_as_uint(__ldcg(src + (size_t)(32 * c + j) * 128));
+                tmem_st_x32(partner_buf + 32 * c, v);
+            }
+            tmem_st_wait();
+            __syncwarp();
+            if (lane == 0)
+                *flag = 0u;  // consumed: no later call can mistake it for its own
+            return true;
+        };
+        for (int64_t i = 0; i < items; ++i) {
+            int64_t t;
+            int kb0, kb1, kind;
+            sk_item_at(sk, pair_id, num_pairs, i, t, kb0, kb1, kind);
             const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
             const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
                                          kSiteEpiAccFull);
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after_sync();
+            const uint32_t acc = tmem_base + lane_base + buf * BNP;
+            if (kind == kItemPieceOut) {
+                // k tail of a tile cut with the previous pair: publish this
+                // CTA's 128 rows, [column][row], and raise this warp's flag
+                float *dst = p.sk_part + (size_t)blockIdx.x * BNP * 128 + 32 * q + lane;
+#pragma unroll 1
+                for (int c = 0; c < BNP / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_x32_sync(acc + 32 * c, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        __stcg(dst + (size_t)(32 * c + j) * 128, __uint_as_float(r[j]));
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    fused::st_release_gpu(p.sk_flags + blockIdx.x * 4 + q, p.epoch);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(acce_leader0 + 8u * buf);
+                if (preload && i == items - 2 && !preload_piece())
+                    break;
+                continue;
+            }
             int64_t mb, nb;
             tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
             const int64_t row0 = mb * BMP + 128 * (int64_t)rank + 32 * q;
@@ -235,12 +315,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (row0 >= p.M || col0 >= p.N)
                     continue;  // warp-uniform: nothing of this chunk is in C
                 uint32_t r[32], h[32];
-                const uint32_t taddr = tmem_base + lane_base + buf * BNP + 64 * c;
+                const uint32_t taddr = acc + 64 * c;
                 tmem_ld_x32_sync(taddr, r);
+                if (kind == kItemPieceIn)
+                    fused::add_tmem(r, partner_buf + 64 * c);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
                 tmem_ld_x32_sync(taddr + 32, r);
+                if (kind == kItemPieceIn)
+                    fused::add_tmem(r, partner_buf + 64 * c + 32);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
@@ -263,7 +347,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0));
+                mbar_arrive_cluster(acce_leader0 + 8u * buf);
+            if (preload && i == items - 2 && !preload_piece())
+                break;
         }
         if (lane == 0)
             bulk_wait_group<0>();

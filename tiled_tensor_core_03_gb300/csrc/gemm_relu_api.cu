@@ -217,10 +217,18 @@ int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensor
     return launch_status(cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p));
 }
 
+// Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
+struct StreamK {
+    int64_t dp_tiles = -1;     // -1: plain data-parallel launch
+    float *part = nullptr;
+    uint32_t *flags = nullptr;
+    uint32_t epoch = 0;
+};
+
 // ---------------------------------------------------------------- CTA-pair launch
 // 256 x 256 tiles on CTA pairs (2-SM MMA).  TMA path only.
 int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                cudaStream_t stream, DeviceState *ds) {
+                cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
     namespace P = gemmrelu::pair;
     namespace F = gemmrelu::fused;
     P::Params p{};
@@ -234,6 +242,10 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
     p.panel = kPanel / 2;                       // same 1024-row panels as the single-CTA kernel
     p.drop_arrive = g_drop_arrive.load();
     p.wait_limit_ns = wait_limit_ns();
+    p.dp_tiles = sk.dp_tiles >= 0 ? sk.dp_tiles : p.num_tiles;
+    p.sk_part = sk.part;
+    p.sk_flags = sk.flags;
+    p.epoch = sk.epoch;
     CUtensorMap mA, mB, mC;
     if (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
         !make_map(&mC, C, M, N, 64, 32))
@@ -241,9 +253,23 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
     if (!ensure_smem_attr(ds->attr_pair, P::gemm_relu_pair_kernel, P::kSmemBytes))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t pairs = std::min<int64_t>(p.num_tiles, ds->sms / 2);
-    P::gemm_relu_pair_kernel<<<(unsigned)(2 * pairs), P::kThreads, P::kSmemBytes, stream>>>(
-        mA, mB, mC, p);
-    return launch_status(cudaGetLastError());
+    if (p.dp_tiles == p.num_tiles) {
+        P::gemm_relu_pair_kernel<<<(unsigned)(2 * pairs), P::kThreads, P::kSmemBytes, stream>>>(
+            mA, mB, mC, p);
+        return launch_status(cudaGetLastError());
+    }
+    // stream-K: pairs wait on flags of their neighbours -> cooperative launch
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(P::kThreads);
+    cfg.dynamicSmemBytes = P::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, P::gemm_relu_pair_kernel, mA, mB, mC, p));
 }
 
 // Whether gemm_relu_f16 runs the CTA-pair kernel: TMA operands, at least one
@@ -261,14 +287,6 @@ bool use_pair(int64_t M, int64_t N, int sms, int path) {
     const int64_t one_waves = ((M + 127) / 128 * ((N + 255) / 256) + sms - 1) / sms;
     return pair_waves <= one_waves;
 }
-
-// Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
-struct StreamK {
-    int64_t dp_tiles = -1;     // -1: plain data-parallel launch
-    float *part = nullptr;
-    uint32_t *flags = nullptr;
-    uint32_t epoch = 0;
-};
 
 int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                  cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
@@ -314,24 +332,38 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
 }
 
 // ---------------------------------------------------------------- stream-K plan
-// For 128 x 256 tiles on a TMA-able problem: when the tiles do not fill a
-// whole number of waves, all but the last full wave run data-parallel and
-// the rest is spread evenly over the grid.  Returns the number of
-// data-parallel tiles, or -1 when stream-K does not apply.
-int64_t streamk_dp_tiles(int64_t M, int64_t N, int sms, int64_t *grid_out) {
-    if (fused_bn(M, N, sms) != 256 || use_pair(M, N, sms, 1))
-        return -1;
-    const int64_t T = ((M + 127) / 128) * ((N + 255) / 256);
-    const int64_t G = std::min<int64_t>(T, sms);
-    if (grid_out)
-        *grid_out = G;
-    if (T <= G || T % G == 0)
-        return -1;
-    return (T / G - 1) * G;
+// When a shape's tiles do not fill a whole number of waves, all full waves
+// but the last run data-parallel and the rest is spread evenly over the
+// workers (CTA pairs for the pair kernel, CTAs for the single-CTA kernel).
+struct SkPlan {
+    bool pair = false;
+    int64_t dp_tiles = -1;     // -1: no stream-K part
+    int64_t ctas = 0;          // workspace slots (one per CTA)
+};
+
+SkPlan streamk_plan(int64_t M, int64_t N, int sms) {
+    SkPlan plan;
+    int64_t T, G;
+    if (use_pair(M, N, sms, 1)) {
+        plan.pair = true;
+        T = ((M + 255) / 256) * ((N + 255) / 256);
+        G = std::min<int64_t>(T, sms / 2);
+        plan.ctas = 2 * G;
+    } else {
+        if (fused_bn(M, N, sms) != 256)
+            return plan;
+        T = ((M + 127) / 128) * ((N + 255) / 256);
+        G = std::min<int64_t>(T, sms);
+        plan.ctas = G;
+    }
+    if (T > G && T % G != 0)
+        plan.dp_tiles = (T / G - 1) * G;
+    return plan;
 }
 
-size_t streamk_bytes(int64_t grid) {
-    return (size_t)grid * 256 * 128 * 4 + (size_t)grid * 4 * 4;
+// Both kernels' slots hold 128 rows x 256 fp32 columns, plus 4 flags.
+size_t streamk_bytes(int64_t ctas) {
+    return (size_t)ctas * 256 * 128 * 4 + (size_t)ctas * 4 * 4;
 }
 
 // ---------------------------------------------------------------- split-K
@@ -482,10 +514,8 @@ size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     DeviceState *ds = nullptr;
     if (current_device_state(&ds) != GEMMRELU_OK)
         return 0;
-    int64_t grid = 0;
-    if (streamk_dp_tiles(M, N, ds->sms, &grid) < 0)
-        return 0;
-    return streamk_bytes(grid);
+    const SkPlan plan = streamk_plan(M, N, ds->sms);
+    return plan.dp_tiles < 0 ? 0 : streamk_bytes(plan.ctas);
 }
 
 int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -502,18 +532,19 @@ int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int6
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return zero_fill(C, M, N, s);
-    int64_t grid = 0;
-    const int64_t dp = streamk_dp_tiles(M, N, ds->sms, &grid);
-    if (dp < 0 || fused_path(A, B, C, M, N, K) != 1)
+    const SkPlan plan = streamk_plan(M, N, ds->sms);
+    if (plan.dp_tiles < 0 || fused_path(A, B, C, M, N, K) != 1)
         return launch_fused(A, B, C, M, N, K, s, ds);
-    if (!workspace || workspace_bytes < streamk_bytes(grid) || !aligned(workspace, 16))
+    if (!workspace || workspace_bytes < streamk_bytes(plan.ctas) || !aligned(workspace, 16))
         return GEMMRELU_ERR_WORKSPACE;
     StreamK sk;
-    sk.dp_tiles = dp;
+    sk.dp_tiles = plan.dp_tiles;
     sk.part = static_cast<float *>(workspace);
     sk.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
-                                            (size_t)grid * 256 * 128 * 4);
+                                            (size_t)plan.ctas * 256 * 128 * 4);
     sk.epoch = next_epoch();
+    if (plan.pair)
+        return launch_pair(A, B, C, M, N, K, s, ds, sk);
     return launch_fused(A, B, C, M, N, K, s, ds, sk);
 }
 

@@ -244,39 +244,56 @@ struct Params {
 
 enum ItemKind : int { kItemFull = 0, kItemPieceOut = 1, kItemPieceIn = 2 };
 
-// Number of work items of CTA c (data-parallel tiles, then stream-K pieces).
-__device__ __forceinline__ int64_t num_items(const Params &p, int64_t c, int64_t G) {
-    const int64_t ndp = c < p.dp_tiles ? (p.dp_tiles - 1 - c) / G + 1 : 0;
-    const int64_t W = (p.num_tiles - p.dp_tiles) * p.num_kb;
+// Stream-K schedule over `num_tiles` tiles of `num_kb` k blocks run by G
+// workers (CTAs, or CTA pairs): tiles [0, dp_tiles) data-parallel, worker c
+// taking c, c + G, ...; the k blocks of the other tiles laid end to end and
+// cut into G equal contiguous ranges.
+struct SkShape {
+    int64_t num_tiles, dp_tiles, num_kb;
+};
+
+// Number of work items of worker c (data-parallel tiles, then pieces).
+__device__ __forceinline__ int64_t sk_num_items(const SkShape &g, int64_t c, int64_t G) {
+    const int64_t ndp = c < g.dp_tiles ? (g.dp_tiles - 1 - c) / G + 1 : 0;
+    const int64_t W = (g.num_tiles - g.dp_tiles) * g.num_kb;
     const int64_t s = c * W / G, e = (c + 1) * W / G;
     if (e <= s)
         return ndp;
-    return ndp + (e - 1) / p.num_kb - s / p.num_kb + 1;
+    return ndp + (e - 1) / g.num_kb - s / g.num_kb + 1;
 }
 
-// Item i of CTA c: tile id, k-block range [kb0, kb1) and kind.  A piece that
-// starts inside its tile is the tile's k tail (kItemPieceOut, stored for the
-// previous CTA); one that stops inside is the k head (kItemPieceIn, adds the
-// next CTA's stored tail).  Each range is at least one tile long, so a piece
-// is never both.
-__device__ __forceinline__ void item_at(const Params &p, int64_t c, int64_t G, int64_t i,
-                                        int64_t &tile, int &kb0, int &kb1, int &kind) {
-    const int64_t ndp = c < p.dp_tiles ? (p.dp_tiles - 1 - c) / G + 1 : 0;
+// Item i of worker c: tile id, k-block range [kb0, kb1) and kind.  A piece
+// that starts inside its tile is the tile's k tail (kItemPieceOut, stored for
+// the previous worker); one that stops inside is the k head (kItemPieceIn,
+// adds the next worker's stored tail).  Each range is at least one tile long,
+// so a piece is never both.
+__device__ __forceinline__ void sk_item_at(const SkShape &g, int64_t c, int64_t G, int64_t i,
+                                           int64_t &tile, int &kb0, int &kb1, int &kind) {
+    const int64_t ndp = c < g.dp_tiles ? (g.dp_tiles - 1 - c) / G + 1 : 0;
     if (i < ndp) {
         tile = c + i * G;
         kb0 = 0;
-        kb1 = p.num_kb;
+        kb1 = (int)g.num_kb;
         kind = kItemFull;
         return;
     }
-    const int64_t W = (p.num_tiles - p.dp_tiles) * p.num_kb;
+    const int64_t W = (g.num_tiles - g.dp_tiles) * g.num_kb;
     const int64_t s = c * W / G, e = (c + 1) * W / G;
-    const int64_t t = s / p.num_kb + (i - ndp);
-    const int64_t lo = t * p.num_kb;
+    const int64_t t = s / g.num_kb + (i - ndp);
+    const int64_t lo = t * g.num_kb;
     kb0 = (int)((s > lo ? s : lo) - lo);
-    kb1 = (int)((e < lo + p.num_kb ? e : lo + p.num_kb) - lo);
-    tile = p.dp_tiles + t;
-    kind = kb0 > 0 ? kItemPieceOut : (kb1 < p.num_kb ? kItemPieceIn : kItemFull);
+    kb1 = (int)((e < lo + g.num_kb ? e : lo + g.num_kb) - lo);
+    tile = g.dp_tiles + t;
+    kind = kb0 > 0 ? kItemPieceOut : (kb1 < g.num_kb ? kItemPieceIn : kItemFull);
+}
+
+__device__ __forceinline__ int64_t num_items(const Params &p, int64_t c, int64_t G) {
+    return sk_num_items(SkShape{p.num_tiles, p.dp_tiles, p.num_kb}, c, G);
+}
+
+__device__ __forceinline__ void item_at(const Params &p, int64_t c, int64_t G, int64_t i,
+                                        int64_t &tile, int &kb0, int &kb1, int &kind) {
+    sk_item_at(SkShape{p.num_tiles, p.dp_tiles, p.num_kb}, c, G, i, tile, kb0, kb1, kind);
 }
 
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
