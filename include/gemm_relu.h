@@ -117,12 +117,19 @@ size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int
  *
  * Follows the split-K scheme of "TileLang 编程基本知识点" section 5.1 (work
  * split over K pieces, each piece offsetting only K) with that page's advice
- * for reproducible results: instead of fp32 atomic adds into C, the call runs
- * two stages on `stream`.  Stage 1 computes each piece's raw fp32 partial
- * (no ReLU) into `workspace`; stage 2 sums the partials in the fixed order
- * 0..split_k-1, applies ReLU and writes fp16 C.  Results are bit-identical
- * from run to run.  Stage 2 is a programmatic dependent launch of stage 1, so
- * it needs no host synchronisation between them.
+ * for reproducible results: instead of fp32 atomic adds into C, every piece's
+ * raw fp32 partial (no ReLU) is kept and the partials are summed in the fixed
+ * order 0..split_k-1 before the ReLU and the fp16 cast.  Results are
+ * bit-identical from run to run, and the same in both forms below:
+ *   - M <= 64 and clamped split_k even, with split_k * R <= 512 (R = 16, 32
+ *     or 64 for M <= 16, <= 32, <= 64): one kernel.  A CTA pair (a
+ *     thread-block cluster of 2) computes the split_k pieces of a tile, half
+ *     each, and continues the ordered sum from one CTA to the other through
+ *     distributed shared memory; no workspace is used (the workspace query
+ *     returns 0).
+ *   - any other clamped split_k: two stages on `stream`.  Stage 1 writes the
+ *     partials to `workspace`; stage 2, a programmatic dependent launch of
+ *     stage 1, sums them, applies ReLU and writes C.
  *
  * The product is computed as C^T = B^T . A^T so that small M maps onto the
  * narrow (N) side of the MMA; this suits skinny, memory-bound shapes.
@@ -131,7 +138,8 @@ size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int
  *            M <= 32); split_k is clamped to the number of such stages.
  * workspace: device buffer of at least
  *            gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes
- *            (split_k * M * N fp32 partials), 16-byte aligned.  Its contents
+ *            (split_k * M * N fp32 partials in the two-stage form), 16-byte
+ *            aligned; may be NULL when that query returns 0.  Its contents
  *            need no initialisation; calls that may run concurrently on the
  *            GPU must use distinct workspaces.
  * Needs A, B 16-byte aligned with K and N multiples of 8 (TMA operands);
@@ -236,6 +244,15 @@ int gemm_relu_debug_set(int drop_arrive, int64_t wait_limit_ns);
  * GEMMRELU_ERR_INVALID_ARG for another value.
  */
 int gemm_relu_debug_force_kernel(int which);
+
+/*
+ * gemm_relu_debug_force_split -- test hook.  0 = gemm_relu_f16_splitk picks
+ * its form as documented there (default); 1 = always the two-stage form (the
+ * workspace query follows the setting).  Both forms give identical bits.
+ * Affects the calling process only.  Returns GEMMRELU_OK, or
+ * GEMMRELU_ERR_INVALID_ARG for another value.
+ */
+int gemm_relu_debug_force_split(int which);
 
 #ifdef __cplusplus
 }

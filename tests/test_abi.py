@@ -94,8 +94,16 @@ def test_rasteriser_panel_order(lib):
 
 
 def test_splitk_workspace_size(lib):
-    # split_k * M * N fp32 partials
-    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 8) == 8 * 16 * 8192 * 4
+    # split 2, 4 or 8 after clamping: reduced inside a cluster, no workspace
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 8) == 0
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 4) == 0
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(64, 128, 600, 4) == 0
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 128, 8192, 32) == 0
+    # M > 64, odd splits, or splits * R > 512: two-stage, split_k * M * N fp32
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(200, 128, 600, 2) == 2 * 200 * 128 * 4
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(64, 128, 8192, 16) == 16 * 64 * 128 * 4
+    # other splits: split_k * M * N fp32 partials
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 3) == 3 * 16 * 8192 * 4
     assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 1) == 0
     # M <= 32 works in 256-wide k stages: K = 600 has 3, so split 8 clamps to 3
     assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 128, 600, 8) == 3 * 16 * 128 * 4
@@ -103,5 +111,13 @@ def test_splitk_workspace_size(lib):
     # 32 < M <= 64 works in 128-wide stages, larger M in 64-wide ones
     assert gr.gemm_relu_f16_splitk_workspace_bytes(64, 128, 600, 8) == 5 * 64 * 128 * 4
     assert gr.gemm_relu_f16_splitk_workspace_bytes(200, 128, 600, 16) == 10 * 200 * 128 * 4
+    # the two-stage form, when forced, always takes a workspace
+    assert gr.gemm_relu_debug_force_split(gr.SPLIT_TWO_STAGE) == gr.OK
+    try:
+        assert gr.gemm_relu_f16_splitk_workspace_bytes(16, 8192, 8192, 8) == 8 * 16 * 8192 * 4
+        assert gr.gemm_relu_f16_splitk_workspace_bytes(64, 128, 600, 4) == 4 * 64 * 128 * 4
+    finally:
+        assert gr.gemm_relu_debug_force_split(gr.SPLIT_AUTO) == gr.OK
+    assert gr.gemm_relu_debug_force_split(2) == gr.ERR_INVALID_ARG
     assert gr.gemm_relu_f16_splitk_workspace_bytes(0, 8, 8, 2) == 0
     assert gr.gemm_relu_f16_splitk_workspace_bytes(8, 8, 8, 0) == 0

@@ -138,7 +138,59 @@ def test_splitk_sweep(orc, M, N, K, S):
     assert gr.status() == gr.OK
 
 
-def test_splitk_deterministic_and_workspace_contents_irrelevant():
+@pytest.fixture
+def two_stage_split():
+    gr.gemm_relu_debug_force_split(gr.SPLIT_TWO_STAGE)
+    yield
+    gr.gemm_relu_debug_force_split(gr.SPLIT_AUTO)
+
+
+# (M, N, K, S): M <= 64 and even splits with S * R <= 512 (R = 16, 32, 64 by
+# M) take the CTA-pair form in automatic mode; every R, ragged M, N and K,
+# S up to 32
+CLUSTER_CASES = [(16, 8192, 8192, 8), (1, 128, 1024, 2), (9, 1032, 3000, 4), (32, 640, 2048, 8),
+                 (40, 264, 1152, 2), (64, 1024, 4096, 8), (61, 520, 960, 4), (16, 256, 8192, 32),
+                 (3, 200, 4096, 6), (30, 1000, 4096, 16), (17, 2056, 1536, 2)]
+
+
+@pytest.mark.parametrize("M,N,K,S", CLUSTER_CASES)
+def test_splitk_cluster_form_matches_two_stage_bits(orc, M, N, K, S):
+    """Both forms add the same S partials in the same order: identical bits."""
+    import torch
+    A, B = inputs.make(M, N, K, dist="normal", scale_by_sqrt_k=True, seed=M + 3 * N + K + S)
+    a, b = dev(A), dev(B)
+    assert gr.gemm_relu_f16_splitk_workspace_bytes(M, N, K, S) == 0
+    c_cluster = gr.gemm_relu_splitk(a, b, S).clone()
+    assert gr.status() == gr.OK
+    gr.gemm_relu_debug_force_split(gr.SPLIT_TWO_STAGE)
+    try:
+        assert gr.gemm_relu_f16_splitk_workspace_bytes(M, N, K, S) == S * M * N * 4
+        c_two = gr.gemm_relu_splitk(a, b, S).clone()
+    finally:
+        gr.gemm_relu_debug_force_split(gr.SPLIT_AUTO)
+    assert gr.status() == gr.OK
+    assert torch.equal(c_cluster.view(torch.int16), c_two.view(torch.int16))
+    rows = sorted({0, M // 2, M - 1})
+    want = np.concatenate([orc.gemm_relu_f16_rows(A, B, r, 1) for r in rows])
+    assert_parity(host(c_cluster)[rows], want, abs_dot(A[rows], B), K, (M, N, K, S))
+
+
+def test_splitk_cluster_form_unaligned_output():
+    """C at a 2-byte offset: the owners fall back to 2-byte stores."""
+    import torch
+    M, N, K, S = 20, 264, 2048, 4
+    A, B = inputs.make(M, N, K, seed=21)
+    a, b = dev(A), dev(B)
+    want = gr.gemm_relu_splitk(a, b, S)
+    buf = torch.full((M * N + 2,), float("nan"), dtype=torch.float16, device="cuda")
+    c = buf[1:1 + M * N].view(M, N)
+    gr.gemm_relu_splitk(a, b, S, out=c)
+    assert gr.status() == gr.OK
+    assert torch.equal(c.view(torch.int16), want.view(torch.int16))
+    assert torch.isnan(buf[0]) and torch.isnan(buf[-1])
+
+
+def test_splitk_deterministic_and_workspace_contents_irrelevant(two_stage_split):
     import torch
     w = inputs.WORKLOADS["skinny"]
     A, B = inputs.make_workload(w)
@@ -208,7 +260,8 @@ def test_output_guard_band_untouched(M, N, K):
     c = buf[pad:pad + M * N].view(M, N)
     gr.gemm_relu(dev(A), dev(B), out=c)
     if K % 8 == 0 and N % 8 == 0:
-        gr.gemm_relu_splitk(dev(A), dev(B), 3, out=c)
+        gr.gemm_relu_splitk(dev(A), dev(B), 3, out=c)      # two-stage form
+        gr.gemm_relu_splitk(dev(A), dev(B), 4, out=c)      # cluster form
     torch.cuda.synchronize()
     assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[pad + M * N:]).all()
     assert not torch.isnan(c).any()

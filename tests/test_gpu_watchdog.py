@@ -23,22 +23,29 @@ def _restore():
     gr.status()
 
 
-@pytest.mark.parametrize("kind", ["tma", "lsu", "splitk"])
+@pytest.mark.parametrize("kind", ["tma", "lsu", "splitk_cluster", "splitk_two_stage"])
 def test_dropped_arrival_times_out_and_recovers(orc, kind):
-    shapes = {"tma": (256, 512, 256), "lsu": (255, 509, 250), "splitk": (16, 1024, 2048)}
+    shapes = {"tma": (256, 512, 256), "lsu": (255, 509, 250), "splitk_cluster": (16, 1024, 2048),
+              "splitk_two_stage": (16, 1024, 2048)}
     M, N, K = shapes[kind]
     A, B = inputs.make(M, N, K, seed=8)
     a, b = dev(A), dev(B)
-    gr.gemm_relu_debug_set(1, 20_000_000)
-    if kind == "splitk":
-        gr.gemm_relu_splitk(a, b, 4)
-    else:
-        gr.gemm_relu(a, b)
-    assert gr.status() == gr.ERR_TIMEOUT
-    assert gr.status() == gr.OK            # reading clears the word
-    gr.gemm_relu_debug_set(0, 0)
-    c = gr.gemm_relu_splitk(a, b, 4) if kind == "splitk" else gr.gemm_relu(a, b)
-    assert gr.status() == gr.OK
+    split = kind.startswith("splitk")
+    if kind == "splitk_two_stage":
+        gr.gemm_relu_debug_force_split(gr.SPLIT_TWO_STAGE)
+    try:
+        gr.gemm_relu_debug_set(1, 20_000_000)
+        if split:
+            gr.gemm_relu_splitk(a, b, 4)
+        else:
+            gr.gemm_relu(a, b)
+        assert gr.status() == gr.ERR_TIMEOUT
+        assert gr.status() == gr.OK            # reading clears the word
+        gr.gemm_relu_debug_set(0, 0)
+        c = gr.gemm_relu_splitk(a, b, 4) if split else gr.gemm_relu(a, b)
+        assert gr.status() == gr.OK
+    finally:
+        gr.gemm_relu_debug_force_split(gr.SPLIT_AUTO)
     assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, kind)
 
 

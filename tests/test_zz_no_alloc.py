@@ -31,17 +31,31 @@ def torch():
     return torch
 
 
+@pytest.fixture
+def split_form(request):
+    """The split-K form under test: the two-stage form is the one that needs
+    scratch; splits of 2, 4 and 8 otherwise reduce inside a cluster and need
+    none."""
+    gr.gemm_relu_debug_force_split(request.param)
+    yield request.param
+    gr.gemm_relu_debug_force_split(gr.SPLIT_AUTO)
+
+
+@pytest.mark.parametrize("split_form", [gr.SPLIT_TWO_STAGE, gr.SPLIT_AUTO], indirect=True,
+                         ids=["two_stage", "auto"])
 @pytest.mark.parametrize("M,N,K,S", [(16, 8192, 8192, 8), (33, 1000, 1000, 3), (1, 128, 1024, 2)])
-def test_noalloc_matches_workspace_entry_point_twice(torch, M, N, K, S):
+def test_noalloc_matches_workspace_entry_point_twice(torch, split_form, M, N, K, S):
     lib = gr.lib()
     A, B = inputs.make(M, N, K, dist="normal", scale_by_sqrt_k=True, seed=M + N + K)
     a = torch.from_numpy(A).cuda()
     b = torch.from_numpy(B).cuda()
     stream = torch.cuda.current_stream().cuda_stream
     need = gr.gemm_relu_f16_splitk_workspace_bytes(M, N, K, S)
-    assert 0 < need <= gr.NOALLOC_SCRATCH_BYTES
+    assert need <= gr.NOALLOC_SCRATCH_BYTES
+    if split_form == gr.SPLIT_TWO_STAGE or S == 3:
+        assert need > 0
 
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
     ref = torch.empty((M, N), dtype=torch.float16, device="cuda")
     rc = lib.gemm_relu_f16_splitk(a.data_ptr(), b.data_ptr(), ref.data_ptr(), M, N, K, S,
                                   ws.data_ptr(), need, stream)
@@ -60,9 +74,11 @@ def test_noalloc_matches_workspace_entry_point_twice(torch, M, N, K, S):
         assert r["finite"] and r["contract_ok"] and r["strict_ok"], (call, r)
 
 
-def test_noalloc_rejects_problems_beyond_its_scratch(torch):
+@pytest.mark.parametrize("split_form,M,S", [(gr.SPLIT_TWO_STAGE, 64, 8), (gr.SPLIT_AUTO, 128, 3)],
+                         indirect=["split_form"], ids=["two_stage", "auto"])
+def test_noalloc_rejects_problems_beyond_its_scratch(torch, split_form, M, S):
     lib = gr.lib()
-    M, N, K, S = 64, 8192, 8192, 8           # needs 16 MiB + counters > 8 MiB
+    N, K = 8192, 8192                        # S * M * 32 KiB of partials > 8 MiB
     assert gr.gemm_relu_f16_splitk_workspace_bytes(M, N, K, S) > gr.NOALLOC_SCRATCH_BYTES
     a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     b = torch.zeros((K, N), dtype=torch.float16, device="cuda")

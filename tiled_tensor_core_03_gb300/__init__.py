@@ -69,6 +69,8 @@ def lib():
         L.gemm_relu_tile_coord.restype = i32
         L.gemm_relu_debug_force_kernel.argtypes = [i32]
         L.gemm_relu_debug_force_kernel.restype = i32
+        L.gemm_relu_debug_force_split.argtypes = [i32]
+        L.gemm_relu_debug_force_split.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
         L.gemm_relu_debug_set.restype = i32
         _lib = L
@@ -134,6 +136,13 @@ KERNEL_AUTO, KERNEL_ONE_CTA_256, KERNEL_ONE_CTA_128, KERNEL_PAIR = 0, 1, 2, 3
 
 def gemm_relu_debug_force_kernel(which):
     return lib().gemm_relu_debug_force_kernel(int(which))
+
+
+SPLIT_AUTO, SPLIT_TWO_STAGE = 0, 1
+
+
+def gemm_relu_debug_force_split(which):
+    return lib().gemm_relu_debug_force_split(int(which))
 
 
 def gemm_relu_debug_set(drop_arrive=0, wait_limit_ns=0):
@@ -217,8 +226,9 @@ def splitk_workspace(M, N, K, split_k, device=None):
 
 def gemm_relu_splitk(a, b, split_k, out=None, workspace=None, stream=None):
     """Same result as gemm_relu, with K split into `split_k` pieces whose fp32
-    partials are reduced in fixed order by a second kernel (for skinny,
-    memory-bound shapes; bit-reproducible)."""
+    partials are summed in fixed order (inside a thread-block cluster for a
+    split of 2, 4 or 8, else by a second kernel) -- for skinny, memory-bound
+    shapes; bit-reproducible."""
     _check_operands(a, b)
     c = _out(a, b, out)
     M, K = a.shape

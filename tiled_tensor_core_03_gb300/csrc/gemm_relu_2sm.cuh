@@ -79,7 +79,7 @@ struct Params {
     // CTA b of a pair cut with the next pair passes its 128 rows of the
     // tile's k tail through sk_part[b] / sk_flags[b][warp] to CTA b - 2.
     int64_t dp_tiles;
-    float *sk_part;        // [2 * pairs][BNP][128] fp32
+    float *sk_part;        // [2 * pairs] slots of 128 x BNP fp32, [BNP/4][128][4]
     uint32_t *sk_flags;    // [2 * pairs][4]
     uint32_t epoch;
 };
@@ -255,16 +255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool got = fused::wait_flag(flag, p.epoch, p.wait_limit_ns, abort_flag);
             if (!__all_sync(0xffffffffu, got))
                 return false;
-            const float *src = p.sk_part + (size_t)(blockIdx.x + 2) * BNP * 128 + 32 * q + lane;
-#pragma unroll 1
-            for (int c = 0; c < BNP / 32; ++c) {
-                uint32_t v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = __float_as_uint(__ldcg(src + (size_t)(32 * c + j) * 128));
-                tmem_st_x32(partner_buf + 32 * c, v);
-            }
-            tmem_st_wait();
+            fused::piece_to_tmem<BNP>(p.sk_part + (size_t)(blockIdx.x + 2) * BNP * 128,
+                                      32 * q + lane, partner_buf);
             __syncwarp();
             if (lane == 0)
                 *flag = 0u;  // consumed: no later call can mistake it for its own
@@ -283,15 +275,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t acc = tmem_base + lane_base + buf * BNP;
             if (kind == kItemPieceOut) {
                 // k tail of a tile cut with the previous pair: publish this
-                // CTA's 128 rows, [column][row], and raise this warp's flag
-                float *dst = p.sk_part + (size_t)blockIdx.x * BNP * 128 + 32 * q + lane;
+                // CTA's 128 rows and raise this warp's flag
+                float *slot = p.sk_part + (size_t)blockIdx.x * BNP * 128;
 #pragma unroll 1
                 for (int c = 0; c < BNP / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_x32_sync(acc + 32 * c, r);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        __stcg(dst + (size_t)(32 * c + j) * 128, __uint_as_float(r[j]));
+                    fused::piece_store32(slot, 32 * q + lane, 32 * c, r);
                 }
                 __threadfence();
                 __syncwarp();

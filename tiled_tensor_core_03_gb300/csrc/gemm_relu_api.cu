@@ -39,6 +39,7 @@ constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;
 std::atomic<int> g_drop_arrive{0};
 std::atomic<int64_t> g_wait_limit_ns{0};
 std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 128, 3 CTA pair
+std::atomic<int> g_force_split{0};    // 0 auto, 1 two-stage split-K form only
 std::atomic<uint32_t> g_epoch{0};
 
 uint32_t next_epoch() {
@@ -58,6 +59,8 @@ struct DeviceState {
     int sms = 0;
     bool attr_fused[4] = {false, false, false, false};
     bool attr_split[4] = {false, false, false, false};
+    bool attr_split_cluster[4] = {false, false, false, false};
+    int split_pairs[4] = {};  // max resident CTA pairs of the cluster form, per bms index
     bool attr_pair = false;
 };
 constexpr int kMaxDevices = 64;
@@ -392,16 +395,27 @@ int effective_splits(int64_t K, int bms, int split_k) {
 
 struct SplitLayout {
     int bms, splits;
+    bool cluster;  // pieces reduced inside a cluster: no workspace, one kernel
     int64_t n_tiles, m_tiles, part_bytes;
 };
+
+// The cluster form splits a tile's S pieces evenly over a CTA pair and keeps
+// one TMEM accumulator per piece, double-buffered: S even and S * BMS <= 512
+// TMEM columns.  It serves M <= 64; for larger M the two-stage form, whose
+// units spread over every SM, measured faster.
+bool split_cluster_ok(int splits, int bms) {
+    return g_force_split.load() == 0 && splits >= 2 && splits % 2 == 0 && splits * bms <= 512 &&
+           bms <= 64;
+}
 
 SplitLayout split_layout(int64_t M, int64_t N, int64_t K, int split_k) {
     SplitLayout L{};
     L.bms = split_bms(M);
     L.splits = effective_splits(K, L.bms, split_k);
+    L.cluster = split_cluster_ok(L.splits, L.bms);
     L.n_tiles = (N + S::BNT - 1) / S::BNT;
     L.m_tiles = (M + L.bms - 1) / L.bms;
-    L.part_bytes = (int64_t)L.splits * M * N * 4;
+    L.part_bytes = L.cluster ? 0 : (int64_t)L.splits * M * N * 4;
     return L;
 }
 
@@ -409,9 +423,9 @@ SplitLayout split_layout(int64_t M, int64_t N, int64_t K, int split_k) {
 // `stream`, so its CTAs can become resident while stage 1 drains.
 int launch_split_reduce(const float *part, void *C, int64_t M, int64_t N, int splits,
                         cudaStream_t stream, DeviceState *ds) {
-    const int64_t groups = M * (N / 8);
+    const int64_t groups = M * (N / 4);
     const int64_t blocks = std::max<int64_t>(
-        1, std::min<int64_t>((groups + 255) / 256, (int64_t)4 * ds->sms));
+        1, std::min<int64_t>((groups + 255) / 256, (int64_t)8 * ds->sms));
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
@@ -422,19 +436,19 @@ int launch_split_reduce(const float *part, void *C, int64_t M, int64_t N, int sp
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int c_vec16 = aligned(C, 16) ? 1 : 0;
+    const int c_vec8 = aligned(C, 8) ? 1 : 0;
     return launch_status(cudaLaunchKernelEx(&cfg, S::gemm_relu_splitk_reduce_kernel, part,
                                             static_cast<uint16_t *>(C), (int)M, (int)N, splits,
-                                            c_vec16));
+                                            c_vec8));
 }
 
 template <int BMS>
 int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                      const SplitLayout &L, void *ws, cudaStream_t stream, DeviceState *ds,
-                     bool &attr_done) {
-    using G = S::Cfg<BMS>;
+                     int bms_index) {
     S::Params p{};
     p.part = static_cast<float *>(ws);
+    p.C = static_cast<uint16_t *>(C);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -442,22 +456,56 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
     p.splits = L.splits;
     p.n_tiles = L.n_tiles;
     p.m_tiles = L.m_tiles;
-    p.num_units = L.n_tiles * L.m_tiles * L.splits;
     p.split_major = kSplitMajor;
     p.drop_arrive = g_drop_arrive.load();
     p.wait_limit_ns = wait_limit_ns();
+    constexpr int kSuperK = S::Cfg<BMS, false>::kSuperK;
     CUtensorMap mA, mB;
-    if (!make_map(&mA, A, M, K, S::BK, BMS) || !make_map(&mB, B, K, N, 64, G::kSuperK))
+    if (!make_map(&mA, A, M, K, S::BK, BMS) || !make_map(&mB, B, K, N, 64, kSuperK))
         return GEMMRELU_ERR_LAUNCH;
-    auto kern = S::gemm_relu_splitk_partial_kernel<BMS>;
-    if (!ensure_smem_attr(attr_done, kern, G::kSmemBytes))
+    if (!L.cluster) {
+        using G = S::Cfg<BMS, false>;
+        p.num_units = L.n_tiles * L.m_tiles * L.splits;
+        auto kern = S::gemm_relu_splitk_kernel<BMS, false>;
+        if (!ensure_smem_attr(ds->attr_split[bms_index], kern, G::kSmemBytes))
+            return GEMMRELU_ERR_LAUNCH;
+        const int64_t grid = std::min<int64_t>(p.num_units, ds->sms);
+        kern<<<(unsigned)grid, 192, G::kSmemBytes, stream>>>(mA, mB, p);
+        const int rc = launch_status(cudaGetLastError());
+        if (rc != GEMMRELU_OK)
+            return rc;
+        return launch_split_reduce(p.part, C, M, N, L.splits, stream, ds);
+    }
+    // cluster form: persistent CTA pairs, one tile at a time each
+    using G = S::Cfg<BMS, true>;
+    p.num_units = L.n_tiles * L.m_tiles;
+    auto kern = S::gemm_relu_splitk_kernel<BMS, true>;
+    if (!ensure_smem_attr(ds->attr_split_cluster[bms_index], kern, G::kSmemBytes))
         return GEMMRELU_ERR_LAUNCH;
-    const int64_t grid = std::min<int64_t>(p.num_units, ds->sms);
-    kern<<<(unsigned)grid, 192, G::kSmemBytes, stream>>>(mA, mB, p);
-    const int rc = launch_status(cudaGetLastError());
-    if (rc != GEMMRELU_OK)
-        return rc;
-    return launch_split_reduce(p.part, C, M, N, L.splits, stream, ds);
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = G::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int &resident = ds->split_pairs[bms_index];
+    if (resident <= 0) {
+        cfg.gridDim = dim3((unsigned)(2 * std::max(1, ds->sms / 2)));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            return GEMMRELU_ERR_LAUNCH;
+        }
+        resident = n;
+    }
+    const int64_t pairs = std::min<int64_t>(p.num_units, resident);
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, mA, mB, p));
 }
 
 // ---------------------------------------------------------------- no-alloc scratch
@@ -577,17 +625,17 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C, int64_t M, int64
     if (L.splits <= 1 || !tma_ok(A, K) || !tma_ok(B, N))
         return launch_fused(A, B, C, M, N, K, s, ds);
     const size_t need = (size_t)L.part_bytes;
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 16))
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return GEMMRELU_ERR_WORKSPACE;
     switch (L.bms) {
     case 16:
-        return launch_split_bms<16>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[0]);
+        return launch_split_bms<16>(A, B, C, M, N, K, L, workspace, s, ds, 0);
     case 32:
-        return launch_split_bms<32>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[1]);
+        return launch_split_bms<32>(A, B, C, M, N, K, L, workspace, s, ds, 1);
     case 64:
-        return launch_split_bms<64>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[2]);
+        return launch_split_bms<64>(A, B, C, M, N, K, L, workspace, s, ds, 2);
     default:
-        return launch_split_bms<128>(A, B, C, M, N, K, L, workspace, s, ds, ds->attr_split[3]);
+        return launch_split_bms<128>(A, B, C, M, N, K, L, workspace, s, ds, 3);
     }
 }
 
@@ -660,6 +708,13 @@ int gemm_relu_debug_force_kernel(int which) {
     if (which < 0 || which > 3)
         return GEMMRELU_ERR_INVALID_ARG;
     g_force_kernel.store(which);
+    return GEMMRELU_OK;
+}
+
+int gemm_relu_debug_force_split(int which) {
+    if (which < 0 || which > 1)
+        return GEMMRELU_ERR_INVALID_ARG;
+    g_force_split.store(which);
     return GEMMRELU_OK;
 }
 

@@ -51,6 +51,7 @@ enum WaitSite : unsigned {
     kSiteEpiAccFull = 4,
     kSiteDrain = 5,
     kSitePieceFlag = 6,
+    kSiteClusterReduce = 7,
 };
 
 __device__ __forceinline__ void record_timeout(volatile uint32_t *abort_flag, unsigned where) {
@@ -69,6 +70,27 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout(abort_flag, where);
+            return false;
+        }
+    }
+}
+
+// wait_bounded for a phase completed by other CTAs of the cluster (acquire
+// at cluster scope, so their shared-memory writes before arriving are seen).
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     uint64_t limit_ns,
+                                                     volatile uint32_t *abort_flag,
+                                                     unsigned where) {
+    if (mbar_try_wait_cluster(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity))
             return true;
         if (*abort_flag)
             return false;
@@ -237,7 +259,7 @@ struct Params {
     // c adds it to its own piece before the ReLU epilogue.  dp_tiles equal to
     // num_tiles means no stream-K part.
     int64_t dp_tiles;
-    float *sk_part;        // [G][BN][BM] fp32 pieces, column-major per slot
+    float *sk_part;        // [G] slots of BM x BN fp32, [BN/4][BM][4] each
     uint32_t *sk_flags;    // [G][4]: one flag per epilogue warp (32 rows)
     uint32_t epoch;        // nonzero, distinct per call
 };
@@ -333,6 +355,50 @@ __device__ __forceinline__ void add_tmem(uint32_t (&r)[32], uint32_t taddr) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
         r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(o[j]));
+}
+
+// A stream-K piece of 128 rows x kCols fp32 columns is kept in its slot as
+// [kCols / 4][128][4]: the four consecutive columns a lane holds for its row
+// are one 16-byte vector, and the 32 rows of a warp are 512 contiguous bytes.
+//
+// piece_store32: store this lane's row, columns col0 .. col0 + 31 (r from a
+// 32-column TMEM load), at L2 (the reader is another SM).
+__device__ __forceinline__ void piece_store32(float *slot, int row, int col0,
+                                              const uint32_t (&r)[32]) {
+    float4 *d = reinterpret_cast<float4 *>(slot) + (size_t)(col0 / 4) * 128 + row;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        __stcg(d + (size_t)i * 128,
+               make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+}
+
+// piece_to_tmem: copy this lane's row of a whole kCols-column piece into TMEM
+// columns taddr .. taddr + kCols - 1.  Four 32-column chunks (32 vector loads)
+// are in flight at once, so the copy costs kCols / 128 L2 round trips.
+template <int kCols>
+__device__ __forceinline__ void piece_to_tmem(const float *slot, int row, uint32_t taddr) {
+    constexpr int kBatch = kCols / 32 < 4 ? kCols / 32 : 4;
+    const float4 *src = reinterpret_cast<const float4 *>(slot) + row;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kCols / 32; c0 += kBatch) {
+        uint32_t v[kBatch][32];
+#pragma unroll
+        for (int cc = 0; cc < kBatch; ++cc) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 x = __ldcg(src + (size_t)((c0 + cc) * 8 + i) * 128);
+                v[cc][4 * i] = __float_as_uint(x.x);
+                v[cc][4 * i + 1] = __float_as_uint(x.y);
+                v[cc][4 * i + 2] = __float_as_uint(x.z);
+                v[cc][4 * i + 3] = __float_as_uint(x.w);
+            }
+        }
+#pragma unroll
+        for (int cc = 0; cc < kBatch; ++cc)
+            tmem_st_x32(taddr + 32 * (c0 + cc), v[cc]);
+    }
+    tmem_st_wait();
 }
 
 template <bool kTma>
@@ -566,16 +632,8 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const bool got = wait_flag(flag, p.epoch, p.wait_limit_ns, abort_flag);
             if (!__all_sync(0xffffffffu, got))
                 return false;
-            const float *src = p.sk_part + (size_t)(blockIdx.x + 1) * BN * BM + 32 * q + lane;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = __float_as_uint(__ldcg(src + (size_t)(32 * c + j) * BM));
-                tmem_st_x32(partner_buf + 32 * c, v);
-            }
-            tmem_st_wait();
+            piece_to_tmem<BN>(p.sk_part + (size_t)(blockIdx.x + 1) * BN * BM, 32 * q + lane,
+                              partner_buf);
             __syncwarp();
             if (lane == 0)
                 *flag = 0u;  // consumed: no later call can mistake it for its own
@@ -596,16 +654,13 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const bool preload_next = preload && i == items - 2;
             if (kind == kItemPieceOut) {
                 // k tail of a tile cut with the previous CTA: publish the raw
-                // fp32 piece in this CTA's slot, [column][row] so that each
-                // warp store covers 32 consecutive rows (128 bytes).
-                float *dst = p.sk_part + (size_t)blockIdx.x * BN * BM + 32 * q + lane;
+                // fp32 piece in this CTA's slot.
+                float *slot = p.sk_part + (size_t)blockIdx.x * BN * BM;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_x32_sync(acc + 32 * c, r);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        __stcg(dst + (size_t)(32 * c + j) * BM, __uint_as_float(r[j]));
+                    piece_store32(slot, 32 * q + lane, 32 * c, r);
                 }
                 __threadfence();
                 __syncwarp();

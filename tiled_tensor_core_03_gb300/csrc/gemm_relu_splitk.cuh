@@ -50,7 +50,10 @@ __host__ __device__ constexpr int kbs_for(int bms) {
                                                    : 1;
 }
 
-template <int BMS>
+// kCluster: a CTA pair (cluster of 2) computes all S pieces of a tile and
+// adds them through distributed shared memory; the second CTA then needs a
+// buffer of BMS x 128 fp32 for the first one's running sum.
+template <int BMS, bool kCluster>
 struct Cfg {
     static constexpr int kKbs = kbs_for(BMS);
     static constexpr int kSuperK = BK * kKbs;               // k per stage
@@ -59,20 +62,22 @@ struct Cfg {
     static constexpr uint32_t kASub = BMS * BK * 2;         // BMS rows x 64 k, K-major
     static constexpr uint32_t kATile = kKbs * kASub;
     static constexpr uint32_t kStageBytes = kBTile + kATile;
-    static constexpr uint32_t kBudget = 227u * 1024u - 1024u - 256u;
+    static constexpr uint32_t kRedBytes = kCluster ? (uint32_t)BMS * BNT * 4u : 0u;
+    static constexpr uint32_t kBudget = 227u * 1024u - 1024u - 256u - kRedBytes;
     static constexpr int kStagesRaw = (int)(kBudget / kStageBytes);
     static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-    static constexpr uint32_t kOffBar = kStages * kStageBytes;
-    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+    static constexpr uint32_t kOffRed = kStages * kStageBytes;
+    static constexpr uint32_t kOffBar = kOffRed + kRedBytes;
+    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1 + 2;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
-    static constexpr uint32_t kTmemCols = (2 * BMS < 32) ? 32 : 2 * BMS;  // power of 2
     // UMMA A (the B tile) N-major: bit 15 = 1; UMMA B (the A tile) K-major.
     static constexpr uint32_t kIdesc = make_idesc_f16_f32(BNT, BMS, 1, 0);
 };
 
 struct Params {
-    float *part;                   // [S][M][N] fp32 partials
+    float *part;                   // [S][M][N] fp32 partials (two-stage form)
+    uint16_t *C;                   // output (cluster form)
     int M, N, K;
     int num_sb, splits;            // super blocks of kSuperK along K; S
     int64_t n_tiles, m_tiles, num_units;
@@ -93,11 +98,23 @@ __device__ __forceinline__ void pdl_wait_primary() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int BMS>
+// One kernel, two forms.
+//   kCluster = false: persistent CTAs walk work units (split s, n tile,
+//     m tile) and write each unit's fp32 partial to part[s][m][n] (stage 1 of
+//     the two-stage form).
+//   kCluster = true (S even): the grid is made of CTA pairs (clusters of 2);
+//     a pair walks tiles, CTA 0 computing pieces 0 .. S/2-1 of each and CTA 1
+//     pieces S/2 .. S-1, every piece into its own TMEM accumulator.  CTA 0
+//     adds its pieces in order, starting from 0, and writes that running sum
+//     into CTA 1's shared memory (remote stores); CTA 1 continues the same
+//     sum with its own pieces in order, applies the ReLU and stores fp16 C.
+//     Every fp32 addition is the one the two-stage form's reduce kernel
+//     makes, in the same order, so both forms give identical bits.
+template <int BMS, bool kCluster>
 __global__ void __launch_bounds__(192, 1)
-    gemm_relu_splitk_partial_kernel(const __grid_constant__ CUtensorMap tmA,
-                                    const __grid_constant__ CUtensorMap tmB, const Params p) {
-    using G = Cfg<BMS>;
+    gemm_relu_splitk_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+    using G = Cfg<BMS, kCluster>;
     constexpr int kStages = G::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -110,12 +127,23 @@ __global__ void __launch_bounds__(192, 1)
     auto accf_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
     auto acce_bar = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    // cluster form: red_full (in CTA 1) completes when CTA 0 has written the
+    // running sum of the current tile; red_empty (in CTA 0) when CTA 1 has
+    // read the previous one.
+    const uint32_t red_full = bar0 + 8u * (2 * kStages + 5);
+    const uint32_t red_empty = bar0 + 8u * (2 * kStages + 6);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + G::kOffMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t S = p.splits;
+    const uint32_t rank = kCluster ? cluster_ctarank() : 0u;
+    // pieces per tile and CTA, each with its own accumulator (x2 buffers)
+    const int pieces = kCluster ? (int)(S / 2) : 1;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < (uint32_t)(2 * pieces * BMS))
+        tmem_cols <<= 1;
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
@@ -127,34 +155,66 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(acce_bar(b), (uint32_t)kEpiWarps);
         }
         mbar_init(drain_bar, 1u);
+        mbar_init(red_full, (uint32_t)kEpiWarps);
+        mbar_init(red_empty, (uint32_t)kEpiWarps);
         *abort_flag = 0u;
         fence_mbar_init();
-        pdl_launch_dependents();
+        fence_proxy_async_smem();  // this thread's TMA copies may use them right away
+        if constexpr (!kCluster)
+            pdl_launch_dependents();
     }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tmA);
-        tma_prefetch_map(&tmB);
+    // Start-up.  The producer warp needs only its own barriers, so it signals
+    // the other warps (named barrier 1) and, in the cluster form, the peer
+    // CTA (cluster barrier), and starts loading at once; the MMA and epilogue
+    // warps wait for the barrier initialisation, the TMEM allocation and --
+    // before any remote access -- the peer's initialisation.
+    uint32_t tmem_base = 0;
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_map(&tmA);
+            tma_prefetch_map(&tmB);
+        }
+        __syncwarp();
+        named_bar_arrive(1, 192);
+        if constexpr (kCluster)
+            cluster_arrive();
+    } else {
+        if (warp == 1) {
+            tmem_alloc(smem_addr(tmem_slot), tmem_cols);
+            tmem_relinquish();
+        }
+        tc_fence_before_sync();
+        named_bar_sync(1, 192);
+        tc_fence_after_sync();
+        if constexpr (kCluster) {
+            cluster_arrive();
+            cluster_wait();
+        }
+        tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     }
-    if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), G::kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
-    // Work unit u -> (split s, n tile, m tile).  Split-major order has
-    // neighbouring CTAs read neighbouring columns of the same rows of B;
+    // Work unit u -> (first piece s, n tile, m tile) and its super blocks
+    // [sb0, sb1).  Two-stage form: one piece per unit; split-major order has
+    // neighbouring CTAs read neighbouring columns of the same rows of B,
     // split-minor order keeps the S pieces of one tile on neighbouring CTAs.
+    // Cluster form: u is the tile, and the CTA's pieces are contiguous in k.
     const int64_t tiles = p.n_tiles * p.m_tiles;
+    const int64_t u_first = kCluster ? (int64_t)(blockIdx.x / 2) : (int64_t)blockIdx.x;
+    const int64_t u_stride = kCluster ? (int64_t)(gridDim.x / 2) : (int64_t)gridDim.x;
+    auto piece_begin = [&](int64_t s) { return (int)((s * p.num_sb) / S); };
     auto unit_coords = [&](int64_t u, int64_t &s, int64_t &nt, int64_t &mt, int &sb0, int &sb1) {
-        s = p.split_major ? u / tiles : u % S;
-        const int64_t tile = p.split_major ? u % tiles : u / S;
+        int64_t tile;
+        if constexpr (kCluster) {
+            s = (int64_t)rank * pieces;
+            tile = u;
+        } else {
+            s = p.split_major ? u / tiles : u % S;
+            tile = p.split_major ? u % tiles : u / S;
+        }
         nt = tile % p.n_tiles;
         mt = tile / p.n_tiles;
-        sb0 = (int)((s * p.num_sb) / S);
-        sb1 = (int)(((s + 1) * p.num_sb) / S);
+        sb0 = piece_begin(s);
+        sb1 = piece_begin(s + pieces);
     };
 
     if (warp == 0) {
@@ -162,7 +222,7 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, parity = 0, issued = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+            for (int64_t u = u_first; ok && u < p.num_units; u += u_stride) {
                 int64_t s, nt, mt;
                 int sb0, sb1;
                 unit_coords(u, s, nt, mt, sb0, sb1);
@@ -174,7 +234,7 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     const bool drop =
-                        p.drop_arrive && blockIdx.x == 0 && u == blockIdx.x && sb == sb0;
+                        p.drop_arrive && blockIdx.x == 0 && u == u_first && sb == sb0;
                     if (!drop) {
                         const uint32_t fb = full_bar(stage);
                         const uint32_t dst = base + stage * G::kStageBytes;
@@ -205,7 +265,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int64_t i = 0;
-            for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++i) {
+            for (int64_t u = u_first; ok && u < p.num_units; u += u_stride, ++i) {
                 int64_t s, nt, mt;
                 int sb0, sb1;
                 unit_coords(u, s, nt, mt, sb0, sb1);
@@ -214,31 +274,37 @@ __global__ void __launch_bounds__(192, 1)
                                   kSiteMmaAccEmpty))
                     break;
                 tc_fence_after_sync();
-                const uint32_t d = tmem_base + buf * BMS;
-                for (int sb = sb0; sb < sb1; ++sb) {
-                    if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
-                                      kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t st = base + stage * G::kStageBytes;
+                for (int j = 0; ok && j < pieces; ++j) {
+                    // piece j of this unit: its own accumulator, started fresh
+                    const int pb0 = piece_begin(s + j), pb1 = piece_begin(s + j + 1);
+                    const uint32_t d = tmem_base + (buf * (uint32_t)pieces + (uint32_t)j) * BMS;
+                    for (int sb = pb0; sb < pb1; ++sb) {
+                        if (!wait_bounded(full_bar(stage), phase, p.wait_limit_ns, abort_flag,
+                                          kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t st = base + stage * G::kStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < G::kSuperK / UK; ++kk) {
-                        // B slab rows are k: the next 16 k are 2 KB further;
-                        // the two 64-wide N slabs are kBSlab apart (LBO).
-                        const uint64_t adesc =
-                            make_sdesc_sw128(st + kk * (UK * 128), G::kBSlab, 1024);
-                        // A: 64-k sub-tile kk / 4, 32 bytes per 16 k inside it.
-                        const uint64_t bdesc = make_sdesc_sw128(
-                            st + G::kBTile + (kk / (BK / UK)) * G::kASub + (kk % (BK / UK)) * (UK * 2),
-                            16, 1024);
-                        umma_f16(d, adesc, bdesc, G::kIdesc, (sb > sb0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(empty_bar(stage));
-                    if (++stage == (uint32_t)kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                        for (int kk = 0; kk < G::kSuperK / UK; ++kk) {
+                            // B slab rows are k: the next 16 k are 2 KB further;
+                            // the two 64-wide N slabs are kBSlab apart (LBO).
+                            const uint64_t adesc =
+                                make_sdesc_sw128(st + kk * (UK * 128), G::kBSlab, 1024);
+                            // A: 64-k sub-tile kk / 4, 32 bytes per 16 k inside it.
+                            const uint64_t bdesc = make_sdesc_sw128(
+                                st + G::kBTile + (kk / (BK / UK)) * G::kASub +
+                                    (kk % (BK / UK)) * (UK * 2),
+                                16, 1024);
+                            umma_f16(d, adesc, bdesc, G::kIdesc,
+                                     (sb > pb0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(empty_bar(stage));
+                        if (++stage == (uint32_t)kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
                 if (!ok)
@@ -253,11 +319,12 @@ __global__ void __launch_bounds__(192, 1)
         // ============================================================ epilogue
         // Lane l of warp q holds output column n = n0 + 32q + l (a TMEM lane)
         // and BMS rows m0.. (TMEM columns); for each row the warp stores 32
-        // consecutive floats (128 B) of part[s][m][*].
+        // consecutive floats (128 B): to part[s][m][*] (two-stage form), or
+        // the pair's running sum to CTA 1's buffer (cluster form, CTA 0).
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         int64_t i = 0;
-        for (int64_t u = blockIdx.x; u < p.num_units; u += gridDim.x, ++i) {
+        for (int64_t u = u_first; u < p.num_units; u += u_stride, ++i) {
             int64_t s, nt, mt;
             int sb0, sb1;
             unit_coords(u, s, nt, mt, sb0, sb1);
@@ -267,6 +334,94 @@ __global__ void __launch_bounds__(192, 1)
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after_sync();
+            if constexpr (kCluster) {
+                // CTA 1's buffer: the running sum over CTA 0's pieces,
+                // [m][n] fp32 (row m of the tile, column n = TMEM lane).
+                const uint32_t red = base + G::kOffRed;
+                const uint32_t n_local = (uint32_t)(32 * q + lane);
+                const uint32_t acc0 = tmem_base + lane_base + buf * (uint32_t)pieces * BMS;
+                if (rank == 0) {
+                    // CTA 1 has read the previous tile's sum
+                    const bool freed = wait_bounded_cluster(red_empty, (uint32_t)((i & 1) ^ 1),
+                                                            p.wait_limit_ns, abort_flag,
+                                                            kSiteClusterReduce);
+                    if (!__all_sync(0xffffffffu, freed))
+                        break;
+                    const uint32_t peer_red = mapa_shared(red, 1u);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BMS; c0 += 16) {
+                        float acc[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            acc[c] = 0.0f;
+#pragma unroll 1
+                        for (int j = 0; j < pieces; ++j) {
+                            uint32_t r[16];
+                            tmem_ld_x16_sync(acc0 + (uint32_t)j * BMS + c0, r);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                acc[c] += __uint_as_float(r[c]);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            st_cluster_f32(peer_red + 4u * ((uint32_t)(c0 + c) * BNT + n_local),
+                                           acc[c]);
+                    }
+                    // accumulators read: hand them back to the MMA warp
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(acce_bar(buf));
+                    // publish: each lane orders its remote stores, the warp
+                    // synchronises, lane 0 signals CTA 1 (release, cluster scope)
+                    fence_acq_rel_cluster();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(red_full, 1u));
+                } else {
+                    const bool full = wait_bounded_cluster(red_full, (uint32_t)(i & 1),
+                                                           p.wait_limit_ns, abort_flag,
+                                                           kSiteClusterReduce);
+                    if (!__all_sync(0xffffffffu, full))
+                        break;
+                    const int64_t col = nt * BNT + n_local;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BMS; c0 += 16) {
+                        float acc[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            acc[c] = __uint_as_float(
+                                ld_shared_b32(red + 4u * ((uint32_t)(c0 + c) * BNT + n_local)));
+#pragma unroll 1
+                        for (int j = 0; j < pieces; ++j) {
+                            uint32_t r[16];
+                            tmem_ld_x16_sync(acc0 + (uint32_t)j * BMS + c0, r);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                acc[c] += __uint_as_float(r[c]);
+                        }
+                        if (col < p.N) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const int64_t m = mt * BMS + c0 + c;
+                                if (m < p.M)
+                                    p.C[m * p.N + col] = (uint16_t)(
+                                        relu_pack_half2(__float_as_uint(acc[c]), 0u) & 0xffffu);
+                            }
+                        }
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(acce_bar(buf));
+                    // buffer read: CTA 0 may write the next tile's sum
+                    fence_acq_rel_cluster();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(red_empty, 0u));
+                }
+                continue;
+            }
             const int64_t n = nt * BNT + 32 * q + lane;
             const int64_t m0 = mt * BMS;
             float *part = p.part + (size_t)s * p.M * p.N;
@@ -293,67 +448,63 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kCluster) {
+        if (warp == 0)
+            cluster_wait();  // the start-up phase the producer only arrived on
+        cluster_sync();      // no CTA leaves while the other may still access its shared memory
+    }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, G::kTmemCols);
+        tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 
 // Stage 2: C[m][n] = fp16(max(part[0][m][n] + part[1][m][n] + ... +
 // part[S-1][m][n], 0)), accumulated in fp32 in exactly that order.  Each
-// thread handles eight consecutive n (N is a multiple of 8 on this path), so
-// loads are 32-byte float4 pairs and the store is one 16-byte vector when C
-// is 16-byte aligned.  Loads of four splits are issued before they are added.
+// thread handles four consecutive n (N is a multiple of 8 on this path): the
+// loads of up to eight splits (one float4 each) are all issued before the
+// first add, so a thread waits for about one memory round trip per eight
+// splits; the store is one 8-byte vector when C is 8-byte aligned.
 __global__ void __launch_bounds__(256)
     gemm_relu_splitk_reduce_kernel(const float *__restrict__ part, uint16_t *__restrict__ C, int M,
-                                   int N, int S, int c_vec16) {
+                                   int N, int S, int c_vec8) {
     pdl_wait_primary();
-    const int64_t per_row = N / 8;
+    const int64_t per_row = N / 4;
     const int64_t groups = (int64_t)M * per_row;
     const size_t split_stride = (size_t)M * (size_t)N;
     for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
         const int64_t m = g / per_row;
-        const int64_t n = (g - m * per_row) * 8;
+        const int64_t n = (g - m * per_row) * 4;
         const float *src = part + m * N + n;
-        float acc[8];
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            float4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            acc[j] = 0.0f;
-        int s = 0;
-        for (; s + 4 <= S; s += 4) {
-            float4 v[4][2];
+            for (int t = 0; t < 8; ++t)
+                v[t] = (s0 + t < S) ? __ldcg(reinterpret_cast<const float4 *>(
+                                          src + (size_t)(s0 + t) * split_stride))
+                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float4 *q = reinterpret_cast<const float4 *>(src + (size_t)(s + t) * split_stride);
-                v[t][0] = __ldcg(q);
-                v[t][1] = __ldcg(q + 1);
-            }
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                acc[0] += v[t][0].x; acc[1] += v[t][0].y; acc[2] += v[t][0].z; acc[3] += v[t][0].w;
-                acc[4] += v[t][1].x; acc[5] += v[t][1].y; acc[6] += v[t][1].z; acc[7] += v[t][1].w;
+            for (int t = 0; t < 8; ++t) {
+                if (s0 + t < S) {
+                    acc.x += v[t].x;
+                    acc.y += v[t].y;
+                    acc.z += v[t].z;
+                    acc.w += v[t].w;
+                }
             }
         }
-        for (; s < S; ++s) {
-            const float4 *q = reinterpret_cast<const float4 *>(src + (size_t)s * split_stride);
-            const float4 a = __ldcg(q), b = __ldcg(q + 1);
-            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-        }
-        uint32_t h[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            h[j] = relu_pack_half2(__float_as_uint(acc[2 * j]), __float_as_uint(acc[2 * j + 1]));
+        const uint32_t h0 = relu_pack_half2(__float_as_uint(acc.x), __float_as_uint(acc.y));
+        const uint32_t h1 = relu_pack_half2(__float_as_uint(acc.z), __float_as_uint(acc.w));
         uint16_t *dst = C + m * N + n;
-        if (c_vec16) {
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+        if (c_vec8) {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(h0, h1);
         } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                dst[2 * j] = (uint16_t)(h[j] & 0xffffu);
-                dst[2 * j + 1] = (uint16_t)(h[j] >> 16);
-            }
+            dst[0] = (uint16_t)(h0 & 0xffffu);
+            dst[1] = (uint16_t)(h0 >> 16);
+            dst[2] = (uint16_t)(h1 & 0xffffu);
+            dst[3] = (uint16_t)(h1 >> 16);
         }
     }
 }
