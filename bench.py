@@ -5,8 +5,11 @@ One step = one pass of the whole hot path over one batch of synthetic input:
      rasteriser, TMA ring, tcgen05 MMA into TMEM, ReLU/fp16 epilogue, with
      the stream-K schedule for the partial last wave;
   2. the split-K kernel on M = 16, N = K = 8192 (N(0,1)/sqrt(K)), split 8:
-     fp32 partials to the workspace, then a fixed-order reduce + ReLU kernel.
-Metric: GEMM+ReLU TFLOP/s = total 2*M*N*K of the step / step time.
+     eight K pieces on CTA pairs, summed in fixed order through shared
+     memory, then ReLU and fp16 (one kernel).
+Metric: GEMM+ReLU TFLOP/s = total 2*M*N*K of the step / step time, the
+steps run back to back on rotating copies of the operands (no L2 reuse
+between launches).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs the same step on its own GPU
@@ -30,19 +33,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # fp16 and bf16 dense tensor rates are the same on this architecture (2.25
 # PFLOP/s nominal each), so the measured bf16 peak is the fp16 denominator.
 FP16_PER_BF16 = 1.0
-L2_FLUSH_BYTES = 512 << 20       # > 129 MB of L2, written between steps
+L2_FLUSH_BYTES = 512 << 20       # > 129 MB of L2, written before each cold launch
 L2_CLEAN_BYTES = 256 << 20       # then read, so no dirty flush lines remain in L2
+INPUT_SETS = 3                   # operand copies each part rotates through
 
 METRIC = "GEMM+ReLU TFLOP/s (fp16 in, fp32 acc)"
 
-# DRAM bytes (read + write) per launch from ncu captures of the current
+# DRAM bytes (read + write) per launch from an ncu capture of the current
 # kernels, keyed by (kind, M, N, K); a shape missing here reports null.
 DRAM_BYTES_PER_LAUNCH = {
-    # profiles/dram_traffic_bench_launches.md (ncu, one launch of each):
-    # pair kernel with stream-K at 4096^3: 75,570,176 B read + 26,821,632 B written
-    ("streamk", 4096, 4096, 4096): 102391808,
-    # split-K partial (134,518,784 + 3,415,552 B) + reduce (4,204,800 + 0 B) at 16x8192x8192
-    ("splitk", 16, 8192, 8192): 142139136,
+    # profiles/dram_traffic_bench_launches.md, first captured launch of each:
+    # pair kernel with stream-K at 4096^3: 76,848,896 B read + 27,169,536 B written
+    ("streamk", 4096, 4096, 4096): 104018432,
+    # split-K CTA-pair form at 16x8192x8192, split 8: 134,519,552 B read + 88,320 B written
+    ("splitk", 16, 8192, 8192): 134607872,
 }
 
 
@@ -266,15 +270,23 @@ def run_ours(args, world, rank, local):
 
     parts, name = build_parts(args)
     host_inputs = {label: inputs.make_workload(w) for label, w, _ in parts}
+    # INPUT_SETS device copies of each part's operands (and outputs): the
+    # back-to-back timed loop rotates through them, so a launch never finds
+    # its operands in L2 -- they were last touched INPUT_SETS steps earlier,
+    # with every other part's traffic in between.
     dev = {}
     for label, w, kind in parts:
         A, B = host_inputs[label]
-        a = torch.from_numpy(A).to(device)
-        b = torch.from_numpy(B).to(device)
-        c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
-        ws = (gr.splitk_workspace(w.M, w.N, w.K, w.split_k, device) if kind == "splitk" else
-              gr.streamk_workspace(w.M, w.N, w.K, device) if kind == "streamk" else None)
-        dev[label] = (a, b, c, ws)
+        sets = []
+        for _ in range(INPUT_SETS):
+            a = torch.from_numpy(A).to(device)
+            b = torch.from_numpy(B).to(device)
+            c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+            ws = (gr.splitk_workspace(w.M, w.N, w.K, w.split_k, device) if kind == "splitk" else
+                  gr.streamk_workspace(w.M, w.N, w.K, device) if kind == "streamk" else None)
+            sets.append((a, b, c, ws))
+        dev[label] = sets
+    set_bytes = sum(w.bytes for _, w, _ in parts)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     clean = torch.ones(L2_CLEAN_BYTES, dtype=torch.uint8, device=device)
 
@@ -287,8 +299,8 @@ def run_ours(args, world, rank, local):
         torch.amax(clean)            # a plain uint8 read: no temporary is written
     stream = torch.cuda.current_stream(device)
 
-    def launch(label, w, kind):
-        a, b, c, ws = dev[label]
+    def launch(label, w, kind, r=0):
+        a, b, c, ws = dev[label][r]
         if kind == "splitk":
             gr.gemm_relu_splitk(a, b, w.split_k, out=c, workspace=ws, stream=stream)
         elif kind == "streamk":
@@ -296,30 +308,32 @@ def run_ours(args, world, rank, local):
         else:
             gr.gemm_relu(a, b, out=c, stream=stream)
 
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
         for p in parts:
             flush_l2()
-            launch(*p)
+            launch(*p, r=i % INPUT_SETS)
     torch.cuda.synchronize(device)
     st = gr.status(stream)
     if st != gr.OK:
         raise RuntimeError(f"device status after warm-up: {gr.strerror(st)}")
 
+    # ---- timed region: K steps back to back, each part on the next input set;
+    # events only at the two ends (an event recorded between two launches
+    # serialises them and would add its own cost to the step)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(parts))]
-          for _ in range(args.steps)]
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(device)
     sampler.mark("t_start")
     wall0 = time.perf_counter()
+    e_start.record(stream)
     for i in range(args.steps):
-        for j, p in enumerate(parts):
-            flush_l2()                   # before every timed launch, outside its events
-            ev[i][2 * j].record(stream)
-            launch(*p)
-            ev[i][2 * j + 1].record(stream)
+        for p in parts:
+            launch(*p, r=i % INPUT_SETS)
+    e_end.record(stream)
     torch.cuda.synchronize(device)
     wall1 = time.perf_counter()
     sampler.mark("t_end")
@@ -328,13 +342,43 @@ def run_ours(args, world, rank, local):
     st = gr.status(stream)
     if st != gr.OK:
         raise RuntimeError(f"device status after timed steps: {gr.strerror(st)}")
-
-    part_ms = {label: [ev[i][2 * j].elapsed_time(ev[i][2 * j + 1]) for i in range(args.steps)]
-               for j, (label, _, _) in enumerate(parts)}
-    step_ms_local = sum(sum(v) for v in part_ms.values()) / args.steps
-    step_ms = max_over_ranks(step_ms_local, world, device)
+    step_ms = max_over_ranks(e_start.elapsed_time(e_end) / args.steps, world, device)
     flops_step = sum(w.flops for _, w, _ in parts)
     value = world * flops_step / (step_ms * 1e-3) / 1e12
+
+    # ---- each part alone: K launches back to back on rotating input sets,
+    # events at both ends -> the kernel's average launch duration
+    part_ms = {}
+    for p in parts:
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        p0.record(stream)
+        for i in range(args.steps):
+            launch(*p, r=i % INPUT_SETS)
+        p1.record(stream)
+        torch.cuda.synchronize(device)
+        part_ms[p[0]] = [p0.elapsed_time(p1) / args.steps]
+    st = gr.status(stream)
+    if st != gr.OK:
+        raise RuntimeError(f"device status after the per-part loops: {gr.strerror(st)}")
+
+    # ---- cold launches: L2 flushed before each, events around each alone
+    cold = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(parts))]
+            for _ in range(args.steps)]
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        for j, p in enumerate(parts):
+            flush_l2()                   # outside the events
+            cold[i][2 * j].record(stream)
+            launch(*p)
+            cold[i][2 * j + 1].record(stream)
+    torch.cuda.synchronize(device)
+    cold_ms = {label: [cold[i][2 * j].elapsed_time(cold[i][2 * j + 1]) for i in range(args.steps)]
+               for j, (label, _, _) in enumerate(parts)}
+    st = gr.status(stream)
+    if st != gr.OK:
+        raise RuntimeError(f"device status after cold launches: {gr.strerror(st)}")
 
     # ---- end to end through the public API, host buffers in pinned memory
     pinned = {}
@@ -346,7 +390,7 @@ def run_ours(args, world, rank, local):
     def e2e_step():
         for label, w, kind in parts:
             hA, hB, hC = pinned[label]
-            a, b, c, _ = dev[label]
+            a, b, c, _ = dev[label][0]
             a.copy_(hA, non_blocking=True)
             b.copy_(hB, non_blocking=True)
             launch(label, w, kind)
@@ -378,9 +422,14 @@ def run_ours(args, world, rank, local):
     hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
 
-    def roofline(label, w, kind):
-        ms = statistics.mean(part_ms[label])
-        kernel = (f"gemm_relu_splitk_partial+reduce {w.M}x{w.N}x{w.K} split {w.split_k}"
+    def split_form(w):
+        one = gr.gemm_relu_f16_splitk_workspace_bytes(w.M, w.N, w.K, w.split_k) == 0
+        return ("CTA-pair form: one kernel, pieces summed in shared memory" if one else
+                "two-stage form: partial kernel + reduce kernel"), (1 if one else 2)
+
+    def roofline(label, w, kind, times):
+        ms = statistics.mean(times[label])
+        kernel = (f"gemm_relu_f16_splitk {w.M}x{w.N}x{w.K} split {w.split_k} ({split_form(w)[0]})"
                   if kind == "splitk" else
                   (f"gemm_relu_f16_streamk {w.M}x{w.N}x{w.K} (CTA-pair or single-CTA fused kernel, "
                    f"as the library selects; stream-K schedule when the tiles leave a partial wave)"
@@ -398,7 +447,8 @@ def run_ours(args, world, rank, local):
                 "peak_source": f"{peaks_src} hbm_gbs",
                 "traffic": DRAM_BYTES_PER_LAUNCH.get((kind, w.M, w.N, w.K))}
 
-    roofs = {label: roofline(label, w, kind) for label, w, kind in parts}
+    roofs = {label: roofline(label, w, kind, part_ms) for label, w, kind in parts}
+    cold_roofs = {label: roofline(label, w, kind, cold_ms) for label, w, kind in parts}
     dominant = max(parts, key=lambda p: sum(part_ms[p[0]]))[0]
     line = {
         "metric": METRIC,
@@ -417,11 +467,19 @@ def run_ours(args, world, rank, local):
             "workload": name,
             "flops_per_step": flops_step,
             "parallelism": f"replicas{world}",
-            "l2": (f"flushed before every timed launch (outside its events) by a "
-                   f"{L2_FLUSH_BYTES >> 20} MiB write followed by a {L2_CLEAN_BYTES >> 20} MiB "
-                   f"read of another buffer: each kernel starts from a cold, clean L2"),
-            "timing": "CUDA events around each launch (split-K: both of its kernels) on the "
-                      "launching stream, summed per step",
+            "l2": (f"inputs larger than L2: every part rotates through {INPUT_SETS} device "
+                   f"copies of its operands ({INPUT_SETS} x {set_bytes / 2**20:.0f} MiB per step "
+                   f"in all), so each launch's A and B were last touched {INPUT_SETS} steps "
+                   f"earlier, behind {(INPUT_SETS - 1) * set_bytes / 2**20:.0f} MiB of other "
+                   f"traffic; no flush inside the timed region. cold_launch: flushed before "
+                   f"every launch by a {L2_FLUSH_BYTES >> 20} MiB write and a "
+                   f"{L2_CLEAN_BYTES >> 20} MiB read of other buffers"),
+            "timing": "steps back to back on one stream, each kernel launched with "
+                      "programmatic stream serialisation; value and ms_per_step from CUDA "
+                      "events at the two ends of the timed region only; parts (and roofline): "
+                      "each part alone, K launches back to back on the rotating input sets, "
+                      "events at both ends; cold_launch: L2 flushed, events around each "
+                      "launch alone (includes the launch latency an idle GPU pays)",
         },
         "roofline": roofs[dominant],
         "parts": {label: {"ms": statistics.mean(part_ms[label]),
@@ -429,13 +487,20 @@ def run_ours(args, world, rank, local):
                           "gbs": w.bytes / (statistics.mean(part_ms[label]) * 1e-3) / 1e9,
                           "roofline": roofs[label]}
                   for label, w, _ in parts},
-        "wall_ms_per_step_incl_flush": 1e3 * (wall1 - wall0) / args.steps,
+        "cold_launch": {label: {"ms": statistics.mean(cold_ms[label]),
+                                "tflops": w.flops / (statistics.mean(cold_ms[label]) * 1e-3) / 1e12,
+                                "gbs": w.bytes / (statistics.mean(cold_ms[label]) * 1e-3) / 1e9,
+                                "frac": cold_roofs[label]["frac"],
+                                "bound": cold_roofs[label]["bound"]}
+                        for label, w, _ in parts},
+        "wall_ms_per_step": 1e3 * (wall1 - wall0) / args.steps,
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "tiled_tensor_core_03_gb300.gemm_relu_streamk / gemm_relu_splitk from pinned host buffers"},
         # this library's kernels in the timed region: the fused kernel once,
-        # split-K as its partial and reduce kernels
-        "gpu_launches": sum(2 if kind == "splitk" else 1 for _, _, kind in parts) * args.steps,
+        # split-K once (CTA-pair form) or twice (partial + reduce)
+        "gpu_launches": sum(split_form(w)[1] if kind == "splitk" else 1
+                            for _, w, kind in parts) * args.steps,
         "clocks": sampler.summary(),
     }
 
@@ -445,7 +510,7 @@ def run_ours(args, world, rank, local):
         err = 0.0
         for label, (rows, want) in outs.items():
             if rows:
-                got = dev[label][2][:rows].cpu().numpy().astype(np.float64)
+                got = dev[label][0][2][:rows].cpu().numpy().astype(np.float64)
                 err = max(err, float(np.abs(got - want.astype(np.float64)).max()))
         desc = ", ".join(f"first {rows} rows of {label}" for label, (rows, _) in outs.items())
         line["cpu_baseline"] = {

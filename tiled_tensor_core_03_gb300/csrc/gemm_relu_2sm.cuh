@@ -122,6 +122,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(drain_bar, 1u);
         *abort_flag = 0u;
         fence_mbar_init();
+        pdl_launch_dependents();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
@@ -136,6 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();          // both CTAs' barriers initialised before any remote signal
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    pdl_wait_primary();      // the previous grid of the stream has completed
 
     if (warp == 0) {
         // ============================================================ producer

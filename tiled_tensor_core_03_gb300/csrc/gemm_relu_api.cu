@@ -14,6 +14,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "gemm_relu.h"
 #include "gemm_relu_kernels.cuh"
@@ -164,6 +165,49 @@ bool ensure_smem_attr(bool &done, Kern kernel, uint32_t bytes) {
     return true;
 }
 
+#ifndef GEMMRELU_PDL
+#define GEMMRELU_PDL 1
+#endif
+
+// Every kernel of this library is launched through here, with programmatic
+// stream serialisation: it may become resident while the previous grid of
+// the stream finishes, overlapping its start-up (barrier set-up, TMEM
+// allocation, descriptor prefetch) with that grid's tail; the kernel waits
+// for the previous grid (griddepcontrol.wait) before it touches global
+// memory.  `cooperative` guarantees co-residency of all CTAs (stream-K);
+// cluster_x > 1 sets a cluster shape at launch.
+template <typename... KArgs, typename... Args>
+int launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block, uint32_t smem,
+                  cudaStream_t stream, bool cooperative, unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[3];
+    unsigned n = 0;
+    if (GEMMRELU_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...));
+}
+
 int zero_fill(void *C, int64_t M, int64_t N, cudaStream_t stream) {
     return launch_status(cudaMemsetAsync(C, 0, (size_t)M * (size_t)N * 2, stream));
 }
@@ -200,24 +244,11 @@ int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensor
     if (!ensure_smem_attr(attr_done, kern, smem))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
-    if (p.dp_tiles == p.num_tiles) {
-        kern<<<(unsigned)grid, F::Roles<kTma>::kThreads, smem, stream>>>(mA, mB, mC, p);
-        return launch_status(cudaGetLastError());
-    }
     // Stream-K: CTAs wait on flags raised by their neighbours, so all of them
     // must be resident at once -- a cooperative launch guarantees that (or
     // fails).
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(F::Roles<kTma>::kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p));
+    return launch_kernel(kern, (unsigned)grid, F::Roles<kTma>::kThreads, smem, stream,
+                         p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p);
 }
 
 // Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
@@ -256,23 +287,9 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
     if (!ensure_smem_attr(ds->attr_pair, P::gemm_relu_pair_kernel, P::kSmemBytes))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t pairs = std::min<int64_t>(p.num_tiles, ds->sms / 2);
-    if (p.dp_tiles == p.num_tiles) {
-        P::gemm_relu_pair_kernel<<<(unsigned)(2 * pairs), P::kThreads, P::kSmemBytes, stream>>>(
-            mA, mB, mC, p);
-        return launch_status(cudaGetLastError());
-    }
     // stream-K: pairs wait on flags of their neighbours -> cooperative launch
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(2 * pairs));
-    cfg.blockDim = dim3(P::kThreads);
-    cfg.dynamicSmemBytes = P::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return launch_status(cudaLaunchKernelEx(&cfg, P::gemm_relu_pair_kernel, mA, mB, mC, p));
+    return launch_kernel(P::gemm_relu_pair_kernel, (unsigned)(2 * pairs), P::kThreads,
+                         P::kSmemBytes, stream, p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p);
 }
 
 // Whether gemm_relu_f16 runs the CTA-pair kernel: TMA operands, at least one
@@ -426,20 +443,9 @@ int launch_split_reduce(const float *part, void *C, int64_t M, int64_t N, int sp
     const int64_t groups = M * (N / 4);
     const int64_t blocks = std::max<int64_t>(
         1, std::min<int64_t>((groups + 255) / 256, (int64_t)8 * ds->sms));
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int c_vec8 = aligned(C, 8) ? 1 : 0;
-    return launch_status(cudaLaunchKernelEx(&cfg, S::gemm_relu_splitk_reduce_kernel, part,
-                                            static_cast<uint16_t *>(C), (int)M, (int)N, splits,
-                                            c_vec8));
+    return launch_kernel(S::gemm_relu_splitk_reduce_kernel, (unsigned)blocks, 256, 0, stream, false,
+                         1, part, static_cast<uint16_t *>(C), (int)M, (int)N, splits, c_vec8);
 }
 
 template <int BMS>
@@ -470,8 +476,8 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
         if (!ensure_smem_attr(ds->attr_split[bms_index], kern, G::kSmemBytes))
             return GEMMRELU_ERR_LAUNCH;
         const int64_t grid = std::min<int64_t>(p.num_units, ds->sms);
-        kern<<<(unsigned)grid, 192, G::kSmemBytes, stream>>>(mA, mB, p);
-        const int rc = launch_status(cudaGetLastError());
+        const int rc = launch_kernel(kern, (unsigned)grid, 192, G::kSmemBytes, stream, false, 1,
+                                     mA, mB, p);
         if (rc != GEMMRELU_OK)
             return rc;
         return launch_split_reduce(p.part, C, M, N, L.splits, stream, ds);
@@ -482,20 +488,19 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
     auto kern = S::gemm_relu_splitk_kernel<BMS, true>;
     if (!ensure_smem_attr(ds->attr_split_cluster[bms_index], kern, G::kSmemBytes))
         return GEMMRELU_ERR_LAUNCH;
-    cudaLaunchConfig_t cfg{};
-    cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = G::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     int &resident = ds->split_pairs[bms_index];
     if (resident <= 0) {
+        cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)(2 * std::max(1, ds->sms / 2)));
+        cfg.blockDim = dim3(192);
+        cfg.dynamicSmemBytes = G::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
@@ -504,8 +509,8 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
         resident = n;
     }
     const int64_t pairs = std::min<int64_t>(p.num_units, resident);
-    cfg.gridDim = dim3((unsigned)(2 * pairs));
-    return launch_status(cudaLaunchKernelEx(&cfg, kern, mA, mB, p));
+    return launch_kernel(kern, (unsigned)(2 * pairs), 192, G::kSmemBytes, stream, false, 2, mA, mB,
+                         p);
 }
 
 // ---------------------------------------------------------------- no-alloc scratch

@@ -450,6 +450,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         mbar_init(drain_bar, 1u);
         *abort_flag = 0u;
         fence_mbar_init();
+        pdl_launch_dependents();
     }
     if (kTma && warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
@@ -464,6 +465,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    pdl_wait_primary();  // the previous grid of the stream has completed
 
     if (warp < R::kLoadWarps) {
         // ============================================================ producer

@@ -86,18 +86,6 @@ struct Params {
     uint64_t wait_limit_ns;
 };
 
-// Let the dependent (reduce) grid launch early; it waits for this grid's
-// completion itself.
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Wait until the grid this one depends on has completed and its memory
-// operations are visible (returns at once without such a dependency).
-__device__ __forceinline__ void pdl_wait_primary() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 // One kernel, two forms.
 //   kCluster = false: persistent CTAs walk work units (split s, n tile,
 //     m tile) and write each unit's fp32 partial to part[s][m][n] (stage 1 of
@@ -160,8 +148,7 @@ __global__ void __launch_bounds__(192, 1)
         *abort_flag = 0u;
         fence_mbar_init();
         fence_proxy_async_smem();  // this thread's TMA copies may use them right away
-        if constexpr (!kCluster)
-            pdl_launch_dependents();
+        pdl_launch_dependents();
     }
     // Start-up.  The producer warp needs only its own barriers, so it signals
     // the other warps (named barrier 1) and, in the cluster form, the peer
@@ -178,6 +165,7 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_arrive(1, 192);
         if constexpr (kCluster)
             cluster_arrive();
+        pdl_wait_primary();  // the previous grid's writes (A, B) are visible
     } else {
         if (warp == 1) {
             tmem_alloc(smem_addr(tmem_slot), tmem_cols);
@@ -191,6 +179,7 @@ __global__ void __launch_bounds__(192, 1)
             cluster_wait();
         }
         tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+        pdl_wait_primary();  // and the previous grid no longer reads C or the workspace
     }
 
     // Work unit u -> (first piece s, n tile, m tile) and its super blocks
@@ -222,6 +211,8 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, parity = 0, issued = 0;
             bool ok = true;
+            // B is read exactly once: stream it through L2 as evict-first
+            const uint64_t stream_once = l2_policy_evict_first();
             for (int64_t u = u_first; ok && u < p.num_units; u += u_stride) {
                 int64_t s, nt, mt;
                 int sb0, sb1;
@@ -240,8 +231,8 @@ __global__ void __launch_bounds__(192, 1)
                         const uint32_t dst = base + stage * G::kStageBytes;
                         const int k0 = sb * G::kSuperK;
                         mbar_arrive_expect_tx(fb, G::kStageBytes);
-                        tma_load_2d(&tmB, dst, fb, n0, k0);
-                        tma_load_2d(&tmB, dst + G::kBSlab, fb, n0 + 64, k0);
+                        tma_load_2d_hint(&tmB, dst, fb, n0, k0, stream_once);
+                        tma_load_2d_hint(&tmB, dst + G::kBSlab, fb, n0 + 64, k0, stream_once);
 #pragma unroll
                         for (int i = 0; i < G::kKbs; ++i)
                             tma_load_2d(&tmA, dst + G::kBTile + i * G::kASub, fb, k0 + i * BK, m0);
@@ -468,6 +459,8 @@ __global__ void __launch_bounds__(192, 1)
 __global__ void __launch_bounds__(256)
     gemm_relu_splitk_reduce_kernel(const float *__restrict__ part, uint16_t *__restrict__ C, int M,
                                    int N, int S, int c_vec8) {
+    if (threadIdx.x == 0)
+        pdl_launch_dependents();
     pdl_wait_primary();
     const int64_t per_row = N / 4;
     const int64_t groups = (int64_t)M * per_row;

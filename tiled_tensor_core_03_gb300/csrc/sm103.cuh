@@ -72,6 +72,26 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap *map, uint32_t dst
         : "memory");
 }
 
+// L2 policy for data read once: its lines are the first to be replaced, so a
+// stream does not push other (for instance dirty) lines out of L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap *map, uint32_t dst,
+                                                 uint32_t bar, int32_t c0, int32_t c1,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1),
+        "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled store shared -> global (elements outside the tensor are skipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src,
                                              int32_t c0, int32_t c1) {
@@ -194,6 +214,24 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[
 // Wait until this thread's tcgen05.st operations have completed.
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation: a grid may
+// become resident while the previous grid of its stream is finishing.  Each
+// kernel lets its own dependent launch early and, after its start-up
+// (barriers, TMEM, descriptor prefetch), waits for the previous grid before
+// it reads or writes global memory.
+
+// Let the next grid of the stream launch (it still waits for this one).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grid this one depends on has completed and its memory
+// operations are visible (returns at once without such a dependency).
+__device__ __forceinline__ void pdl_wait_primary() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- CTA pairs (2-SM MMA)
