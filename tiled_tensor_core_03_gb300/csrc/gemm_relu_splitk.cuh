@@ -1,26 +1,28 @@
 // gemm_relu_splitk.cuh -- split-K fused GEMM + ReLU for skinny (memory-bound)
-// shapes, in two stages.
+// shapes.
 //
 // The split-K scheme of "TileLang 编程基本知识点" section 5.1 cuts the K range
 // into S pieces computed by different CTAs; each piece only offsets K.  The
 // page adds the fp32 partials with atomics into a pre-zeroed C, and notes
-// that for reproducible results the partials should instead be written to a
-// workspace and reduced in a separate step.  That is what happens here:
+// that for reproducible results the partials should instead be kept and
+// reduced in a separate step.  Here the S raw fp32 partials (no ReLU) are
+// always summed in the fixed order 0, 1, ..., S-1 starting from 0, then the
+// ReLU and the fp16 cast follow, in one of two forms:
 //
-//   stage 1  gemm_relu_splitk_partial_kernel: C^T = B^T . A^T per piece.  The
-//            MMA's M side (128 TMEM lanes) runs over N and its narrow N side
-//            (BMS columns) over M, so M = 16 costs a 128 x 16 MMA instead of
-//            a mostly empty 128-row tile.  UMMA A operand = a B tile,
-//            N-major; UMMA B operand = an A tile, K-major.  Each work unit
-//            (split s, n tile, m tile) writes its raw fp32 partial (no ReLU)
-//            to part[s][m][n].
-//   stage 2  gemm_relu_splitk_reduce_kernel: C[m][n] = fp16(max(sum over
-//            s = 0..S-1 of part[s][m][n], 0)), summed in that fixed order, so
-//            the result is bit-identical from run to run.
+//   CTA-pair form (gemm_relu_splitk_kernel<BMS, true>): a cluster of two
+//     CTAs computes all pieces of a tile, half each, one TMEM accumulator
+//     per piece; the first CTA's running sum moves to the second through
+//     distributed shared memory and the second finishes the sum and stores
+//     C.  One kernel, no workspace.
+//   two-stage form: gemm_relu_splitk_kernel<BMS, false> writes every
+//     piece's partial to part[s][m][n]; gemm_relu_splitk_reduce_kernel, a
+//     programmatic dependent launch, sums them and stores C.
 //
-// Stage 2 is launched as a programmatic dependent of stage 1: its CTAs
-// become resident as stage-1 CTAs retire and wait (griddepcontrol.wait)
-// until stage 1 has completed and its writes are visible.
+// Both compute C^T = B^T . A^T: the MMA's M side (128 TMEM lanes) runs over
+// N and its narrow N side (BMS columns) over M, so M = 16 costs a 128 x 16
+// MMA instead of a mostly empty 128-row tile.  UMMA A operand = a B tile,
+// N-major; UMMA B operand = an A tile, K-major.  Both forms make the same
+// fp32 additions in the same order, so they give identical bits.
 #pragma once
 
 #include <cuda_fp16.h>
