@@ -474,7 +474,9 @@ def run_ours(args, world, rank, local):
                   if kind == "splitk" else
                   (f"gemm_relu_f16_streamk {w.M}x{w.N}x{w.K} (CTA-pair or single-CTA fused kernel, "
                    f"as the library selects; stream-K schedule when the tiles leave a partial wave)"
-                   if kind == "streamk" else f"gemm_relu_f16 {w.M}x{w.N}x{w.K}"))
+                   if kind == "streamk" and w.M > 4 else
+                   f"gemm_relu_f16 {w.M}x{w.N}x{w.K} (GEMV kernel, M <= 4)" if w.M <= 4 else
+                   f"gemm_relu_f16 {w.M}x{w.N}x{w.K}"))
         if w.flops / w.bytes >= ridge:
             ach = w.flops / (ms * 1e-3) / 1e12
             return {"bound": "tensor", "kernel": kernel, "achieved": ach, "peak": tensor_peak,
@@ -580,7 +582,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of wall time for the cpu_baseline sample")
     ap.add_argument("--workload", default="step",
-                    choices=["step", "square256", "square1024", "ragged", "square4096", "skinny"])
+                    choices=["step", "square256", "square1024", "ragged", "square4096", "skinny",
+                             "decode1"])
     ap.add_argument("--shape", default=None, help="MxNxK: one custom fused (or split) GEMM")
     ap.add_argument("--split", type=int, default=1, help="split-K for --shape")
     ap.add_argument("--no-streamk", action="store_true",

@@ -57,11 +57,23 @@ typedef enum {
 /*
  * gemm_relu_f16 -- C = fp16(max(A . B, 0)).
  *
- * One fused kernel: TMA (or predicated loads) into a multistage shared-memory
- * ring, tcgen05.mma into a TMEM fp32 accumulator, ReLU + fp16 cast in the
- * epilogue, TMA (or predicated) stores.  Tiles of 128 x 256 outputs (128 x
- * 128 when that fills the SMs in fewer waves, e.g. 1024^3), a persistent grid
- * of at most one CTA per SM, grouped (L2-friendly) tile order.
+ * One fused kernel, chosen per shape:
+ *   - M >= 256 and N >= 256 with TMA-capable A, B, C: 256 x 256 tiles on CTA
+ *     pairs (tcgen05.mma.cta_group::2), when that needs no more waves than
+ *     one CTA per 128 x 256 tile;
+ *   - M <= 4 with TMA-capable A and B: the GEMV kernel -- B streamed through
+ *     shared memory, fp32 multiply-adds on the CUDA cores, K chunks reduced
+ *     in a fixed order inside a thread-block cluster (the GEMV pattern of
+ *     "TileLang CUDA 核心编程模式" section 4);
+ *   - M <= 64 with TMA-capable A and B whose 128 x 256 tiles would keep
+ *     fewer than half of the SMs busy: gemm_relu_f16_splitk's CTA-pair form
+ *     with split_k = 2 (one kernel, no workspace; identical bits to that
+ *     call);
+ *   - otherwise one CTA per 128 x 256 (or 128 x 128) tile: TMA (or predicated
+ *     loads) into a multistage shared-memory ring, tcgen05.mma into a TMEM
+ *     fp32 accumulator, ReLU + fp16 cast in the epilogue, TMA (or
+ *     predicated) stores; persistent grid, grouped (L2-friendly) tile order.
+ * Every choice sums in a fixed order: the same call gives the same bits.
  *
  * Returns GEMMRELU_OK or an error code; asynchronous on `stream`.
  */
@@ -239,8 +251,9 @@ int gemm_relu_debug_set(int drop_arrive, int64_t wait_limit_ns);
  * gemm_relu_f16 (and the unsplit fallbacks of the other entry points) runs:
  * 0 = automatic choice (default), 1 = one CTA per 128 x 256 tile, 2 = one CTA
  * per 128 x 128 tile, 3 = CTA pairs on 256 x 256 tiles (TMA operands only;
- * others take the one-CTA kernel).  All give results within the same
- * tolerance.  Affects the calling process only.  Returns GEMMRELU_OK, or
+ * others take the one-CTA kernel), 4 = the GEMV kernel where it applies
+ * (M <= 8, TMA-capable A and B; else the automatic choice).  All give
+ * results within the same tolerance.  Affects the calling process only.  Returns GEMMRELU_OK, or
  * GEMMRELU_ERR_INVALID_ARG for another value.
  */
 int gemm_relu_debug_force_kernel(int which);

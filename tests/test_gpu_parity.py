@@ -29,7 +29,7 @@ def _cuda():
 # ----------------------------------------------------------------- workloads
 
 
-@pytest.mark.parametrize("name", ["square256", "square1024", "ragged"])
+@pytest.mark.parametrize("name", ["square256", "square1024", "ragged", "decode1"])
 def test_workload_full(orc, name):
     w = inputs.WORKLOADS[name]
     A, B = inputs.make_workload(w)
@@ -388,3 +388,70 @@ def test_pair_integer_inputs_bit_exact(orc, forced_kernel):
         B = rng.integers(-4, 5, (K, N)).astype(np.float16)
         assert np.array_equal(run_fused(A, B).astype(np.float64),
                               orc.gemm_relu_f16(A, B).astype(np.float64))
+
+
+# ----------------------------------------------------------------- GEMV (M <= 8)
+
+# (M, N, K): every accumulator width (1, 2, 4, 8 rows), M between them, ragged N
+# (not a multiple of the 256-column block) and K (not a multiple of 32),
+# cluster sizes 1..8
+GEMV_CASES = [(1, 8, 8), (1, 8192, 8192), (2, 264, 72), (3, 520, 1000), (4, 136, 4096),
+              (5, 1032, 2056), (7, 256, 40), (8, 8192, 1024), (8, 2048, 8200), (6, 16392, 512)]
+
+
+@pytest.fixture
+def forced_gemv():
+    gr.gemm_relu_debug_force_kernel(gr.KERNEL_GEMV)
+    yield
+    gr.gemm_relu_debug_force_kernel(gr.KERNEL_AUTO)
+
+
+@pytest.mark.parametrize("M,N,K", GEMV_CASES)
+def test_gemv_parity(orc, forced_gemv, M, N, K):
+    import torch
+    A, B = inputs.make(M, N, K, dist="normal", scale_by_sqrt_k=True, seed=M * 31 + N + K)
+    a, b = dev(A), dev(B)
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    assert gr.gemm_relu_f16_path(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K) == gr.PATH_TMA
+    gr.gemm_relu(a, b, out=c)
+    assert gr.status() == gr.OK
+    assert_parity(host(c), orc.gemm_relu_f16(A, B), abs_dot(A, B), K, (M, N, K))
+    again = gr.gemm_relu(a, b)
+    assert torch.equal(c.view(torch.int16), again.view(torch.int16))      # fixed order
+
+
+def test_gemv_integer_inputs_bit_exact(orc, forced_gemv):
+    """Small integers: every partial sum is exact in fp32, so GEMV, oracle and
+    exact arithmetic agree bit for bit, over all eight rows and ragged tiles."""
+    rng = np.random.default_rng(3)
+    M, N, K = 8, 776, 1000
+    A = rng.integers(-4, 5, (M, K)).astype(np.float16)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float16)
+    got = run_fused(A, B).astype(np.float64)
+    assert np.array_equal(got, orc.gemm_relu_f16(A, B).astype(np.float64))
+
+
+def test_decode_rows_routing(orc):
+    """gemm_relu_f16 on decode-like rows: M <= 4 runs the GEMV kernel (same
+    bits as forcing it); M = 8 with few column tiles runs K split in two on
+    CTA pairs (same bits as gemm_relu_f16_splitk with split 2); both agree
+    with the oracle and with the tensor-core tile kernel within the bounds."""
+    import torch
+    for M, N, K in [(4, 4096, 4096), (8, 4096, 4096)]:
+        A, B = inputs.make(M, N, K, dist="uniform", seed=70 + M)
+        a, b = dev(A), dev(B)
+        auto = gr.gemm_relu(a, b)
+        try:
+            gr.gemm_relu_debug_force_kernel(gr.KERNEL_GEMV)
+            gemv = gr.gemm_relu(a, b)
+            gr.gemm_relu_debug_force_kernel(gr.KERNEL_ONE_CTA_256)
+            tile = gr.gemm_relu(a, b)
+        finally:
+            gr.gemm_relu_debug_force_kernel(gr.KERNEL_AUTO)
+        split2 = gr.gemm_relu_splitk(a, b, 2)
+        assert gr.status() == gr.OK
+        same = gemv if M <= 4 else split2
+        assert torch.equal(auto.view(torch.int16), same.view(torch.int16)), M
+        want = orc.gemm_relu_f16(A, B)
+        for name, got in (("auto", auto), ("gemv", gemv), ("tile", tile), ("split2", split2)):
+            assert_parity(host(got), want, abs_dot(A, B), K, (M, name))

@@ -23,10 +23,10 @@ def _restore():
     gr.status()
 
 
-@pytest.mark.parametrize("kind", ["tma", "lsu", "splitk_cluster", "splitk_two_stage"])
+@pytest.mark.parametrize("kind", ["tma", "lsu", "gemv", "splitk_cluster", "splitk_two_stage"])
 def test_dropped_arrival_times_out_and_recovers(orc, kind):
-    shapes = {"tma": (256, 512, 256), "lsu": (255, 509, 250), "splitk_cluster": (16, 1024, 2048),
-              "splitk_two_stage": (16, 1024, 2048)}
+    shapes = {"tma": (256, 512, 256), "lsu": (255, 509, 250), "gemv": (4, 2048, 2048),
+              "splitk_cluster": (16, 1024, 2048), "splitk_two_stage": (16, 1024, 2048)}
     M, N, K = shapes[kind]
     A, B = inputs.make(M, N, K, seed=8)
     a, b = dev(A), dev(B)

@@ -131,7 +131,7 @@ def gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel):
     return mb.value, nb.value
 
 
-KERNEL_AUTO, KERNEL_ONE_CTA_256, KERNEL_ONE_CTA_128, KERNEL_PAIR = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_ONE_CTA_256, KERNEL_ONE_CTA_128, KERNEL_PAIR, KERNEL_GEMV = 0, 1, 2, 3, 4
 
 
 def gemm_relu_debug_force_kernel(which):

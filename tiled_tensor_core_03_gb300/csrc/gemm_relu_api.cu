@@ -20,6 +20,7 @@
 #include "gemm_relu_kernels.cuh"
 #include "gemm_relu_splitk.cuh"
 #include "gemm_relu_2sm.cuh"
+#include "gemm_relu_gemv.cuh"
 
 namespace {
 
@@ -39,7 +40,8 @@ constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;
 // ---------------------------------------------------------------- test hooks
 std::atomic<int> g_drop_arrive{0};
 std::atomic<int64_t> g_wait_limit_ns{0};
-std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 128, 3 CTA pair
+std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 128, 3 CTA pair,
+                                      // 4 GEMV (M <= 8)
 std::atomic<int> g_force_split{0};    // 0 auto, 1 two-stage split-K form only
 std::atomic<uint32_t> g_epoch{0};
 
@@ -63,6 +65,7 @@ struct DeviceState {
     bool attr_split_cluster[4] = {false, false, false, false};
     int split_pairs[4] = {};  // max resident CTA pairs of the cluster form, per bms index
     bool attr_pair = false;
+    bool attr_gemv[4] = {false, false, false, false};
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -109,9 +112,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // Row-major fp16 matrix rows x cols (cols contiguous), box box_cols x box_rows,
-// 128-byte swizzle, zero fill outside the matrix.
+// 128-byte swizzle (or none), zero fill outside the matrix.
 bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
-              uint32_t box_rows) {
+              uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
@@ -120,7 +123,7 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, uin
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -292,6 +295,69 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
                          P::kSmemBytes, stream, p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p);
 }
 
+// ---------------------------------------------------------------- GEMV (M <= 8)
+namespace V = gemmrelu::gemv;
+
+// Whether a plain (unsplit, not stream-K) launch runs the GEMV kernel: TMA-
+// capable A and B and at most four rows (eight when forced).  Measured on
+// GB300 at N = K = 8192: M = 1, 2, 4 stream B at 5.3, 5.1, 4.9 TB/s; at M = 8
+// the multiply-adds, not HBM, set the pace (37 us) and the tensor-core split
+// below is faster (29 us).
+constexpr int64_t kGemvMaxM = 4;
+
+bool use_gemv(const void *A, const void *B, int64_t M, int64_t N, int64_t K) {
+    const int force = g_force_kernel.load();
+    if (force != 0 && force != 4)
+        return false;
+    return M <= (force == 4 ? (int64_t)V::kMaxM : kGemvMaxM) && tma_ok(A, K) && tma_ok(B, N);
+}
+
+// K chunks per column block (the cluster size): doubled while the grid stays
+// within two CTAs per SM and every chunk keeps at least four 32-row stages.
+int gemv_csize(int64_t N, int64_t K, int sms) {
+    const int64_t blocks = (N + V::kCols - 1) / V::kCols;
+    const int64_t stages = (K + V::kRows - 1) / V::kRows;
+    int c = 1;
+    while (c < V::kMaxCluster && blocks * c * 2 <= 2 * (int64_t)sms && stages >= (int64_t)c * 2 * 4)
+        c *= 2;
+    return c;
+}
+
+template <int MV>
+int launch_gemv_mv(const CUtensorMap &mA, const CUtensorMap &mB, const V::Params &p, int csize,
+                   int64_t blocks, cudaStream_t stream, bool &attr_done) {
+    auto kern = V::gemm_relu_gemv_kernel<MV>;
+    if (!ensure_smem_attr(attr_done, kern, V::kSmemBytes))
+        return GEMMRELU_ERR_LAUNCH;
+    return launch_kernel(kern, (unsigned)(blocks * csize), V::kThreads, V::kSmemBytes, stream,
+                         false, (unsigned)csize, mA, mB, p, csize);
+}
+
+int launch_gemv(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                cudaStream_t stream, DeviceState *ds) {
+    V::Params p{};
+    p.C = static_cast<uint16_t *>(C);
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.num_stages = (int)((K + V::kRows - 1) / V::kRows);
+    p.drop_arrive = g_drop_arrive.load();
+    p.wait_limit_ns = wait_limit_ns();
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, M, K, V::kRows, V::kMaxM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&mB, B, K, N, V::kCols, V::kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GEMMRELU_ERR_LAUNCH;
+    const int csize = gemv_csize(N, K, ds->sms);
+    const int64_t blocks = (N + V::kCols - 1) / V::kCols;
+    if (M <= 1)
+        return launch_gemv_mv<1>(mA, mB, p, csize, blocks, stream, ds->attr_gemv[0]);
+    if (M <= 2)
+        return launch_gemv_mv<2>(mA, mB, p, csize, blocks, stream, ds->attr_gemv[1]);
+    if (M <= 4)
+        return launch_gemv_mv<4>(mA, mB, p, csize, blocks, stream, ds->attr_gemv[2]);
+    return launch_gemv_mv<8>(mA, mB, p, csize, blocks, stream, ds->attr_gemv[3]);
+}
+
 // Whether gemm_relu_f16 runs the CTA-pair kernel: TMA operands, at least one
 // full 256 x 256 tile, and no more weighted waves than the single-CTA choice
 // (a 256 x 256 pair tile does the work of two 128 x 256 tiles on two SMs).
@@ -308,10 +374,18 @@ bool use_pair(int64_t M, int64_t N, int sms, int path) {
     return pair_waves <= one_waves;
 }
 
+int launch_skinny_split(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream, DeviceState *ds);
+bool use_skinny_split(const void *A, const void *B, int64_t M, int64_t N, int64_t K, int sms);
+
 int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                  cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
     namespace F = gemmrelu::fused;
     const int path = fused_path(A, B, C, M, N, K);
+    if (sk.dp_tiles < 0 && use_gemv(A, B, M, N, K))
+        return launch_gemv(A, B, C, M, N, K, stream, ds);
+    if (sk.dp_tiles < 0 && use_skinny_split(A, B, M, N, K, ds->sms))
+        return launch_skinny_split(A, B, C, M, N, K, stream, ds);
     if (sk.dp_tiles < 0 && use_pair(M, N, ds->sms, path))
         return launch_pair(A, B, C, M, N, K, stream, ds);
     F::Params p{};
@@ -364,6 +438,8 @@ struct SkPlan {
 SkPlan streamk_plan(int64_t M, int64_t N, int sms) {
     SkPlan plan;
     int64_t T, G;
+    if (M <= V::kMaxM)
+        return plan;  // decode-like rows: the GEMV kernel (or the plain one) serves them
     if (use_pair(M, N, sms, 1)) {
         plan.pair = true;
         T = ((M + 255) / 256) * ((N + 255) / 256);
@@ -511,6 +587,36 @@ int launch_split_bms(const void *A, const void *B, void *C, int64_t M, int64_t N
     const int64_t pairs = std::min<int64_t>(p.num_units, resident);
     return launch_kernel(kern, (unsigned)(2 * pairs), 192, G::kSmemBytes, stream, false, 2, mA, mB,
                          p);
+}
+
+// ---------------------------------------------------------------- skinny shapes
+// A plain launch of a skinny shape (M <= 64) whose 128 x 256 tiles would keep
+// fewer than half of the SMs busy runs as a split of K in two, in the
+// CTA-pair form: two CTAs per 128-column tile, each streaming half of K, the
+// halves added in a fixed order on chip -- one kernel, no workspace.
+bool use_skinny_split(const void *A, const void *B, int64_t M, int64_t N, int64_t K, int sms) {
+    if (g_force_kernel.load() != 0 || g_force_split.load() != 0 || M > 64)
+        return false;
+    if (!tma_ok(A, K) || !tma_ok(B, N))
+        return false;
+    const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+    if (2 * tiles > sms)
+        return false;
+    const SplitLayout L = split_layout(M, N, K, 2);
+    return L.splits == 2 && L.cluster;
+}
+
+int launch_skinny_split(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream, DeviceState *ds) {
+    const SplitLayout L = split_layout(M, N, K, 2);
+    switch (L.bms) {
+    case 16:
+        return launch_split_bms<16>(A, B, C, M, N, K, L, nullptr, stream, ds, 0);
+    case 32:
+        return launch_split_bms<32>(A, B, C, M, N, K, L, nullptr, stream, ds, 1);
+    default:
+        return launch_split_bms<64>(A, B, C, M, N, K, L, nullptr, stream, ds, 2);
+    }
 }
 
 // ---------------------------------------------------------------- no-alloc scratch
@@ -710,7 +816,7 @@ int gemm_relu_tile_coord(int64_t tile, int64_t m_tiles, int64_t n_tiles, int pan
 }
 
 int gemm_relu_debug_force_kernel(int which) {
-    if (which < 0 || which > 3)
+    if (which < 0 || which > 4)
         return GEMMRELU_ERR_INVALID_ARG;
     g_force_kernel.store(which);
     return GEMMRELU_OK;

@@ -51,6 +51,8 @@ WORKLOADS = {
         Workload("ragged", 1537, 1023, 777, "uniform", False, 2),
         Workload("square4096", 4096, 4096, 4096, "normal", True, 3),
         Workload("skinny", 16, 8192, 8192, "normal", True, 4, split_k=8),
+        # the skinny shape taken to one row (a decode step): the GEMV path
+        Workload("decode1", 1, 8192, 8192, "normal", True, 5),
     ]
 }
 
