@@ -1,11 +1,13 @@
-"""CPU oracle for C = fp16(max(A . B, 0)) -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracles for C = fp16(max(A . B, 0)) and for attention forward
+O = fp16(softmax(Q K^T / sqrt(d)) V) -- TEST INFRASTRUCTURE ONLY.
 
 Only the tests, the package entry point's smoke check and the benchmark's
 CPU-baseline leg may import this package.  The product path (the CUDA library
 and its Python binding) never imports, links or executes it.
 
 The arithmetic lives in gemm_relu_oracle.c (fp64 triple loop, ReLU on the
-accumulator, one round-to-nearest-even to binary16); this module only
+accumulator, one round-to-nearest-even to binary16) and attention_oracle.c
+(fp64 scores, softmax and weighted sum of V, one rounding); this module only
 marshals numpy arrays through ctypes.
 """
 import ctypes
@@ -45,6 +47,11 @@ def _bind(lib):
     lib.oracle_gemm_relu_f16_rows.restype = None
     lib.oracle_gemm_relu_f16_at.argtypes = [p, p, i64, i64, i64, p, p, i64, p]
     lib.oracle_gemm_relu_f16_at.restype = None
+    lib.oracle_attention_f16.argtypes = [p, p, p, p, i64, i64, i64, i64, ctypes.c_int]
+    lib.oracle_attention_f16.restype = None
+    lib.oracle_attention_f16_rows.argtypes = [p, p, p, p, i64, i64, i64, ctypes.c_int,
+                                              i64, i64, i64, i64]
+    lib.oracle_attention_f16_rows.restype = None
     return lib
 
 
@@ -110,3 +117,26 @@ class Oracle:
         self.lib.oracle_gemm_relu_f16_at(_ptr(A), _ptr(B), M, N, K, _ptr(I), _ptr(J),
                                          I.size, _ptr(out))
         return out.view(np.float16)
+
+    # ------------------------------------------------------------ attention
+
+    def attention_f16(self, Q, K, V, causal):
+        """O = fp16(softmax(Q K^T / sqrt(d)) V) for [batch, seq, heads, dim] fp16
+        arrays (key j visible to query i iff j <= i when causal)."""
+        Q, K, V = _h(Q), _h(K), _h(V)
+        assert Q.ndim == 4 and Q.shape == K.shape == V.shape, (Q.shape, K.shape, V.shape)
+        b, s, h, d = Q.shape
+        O = np.empty_like(Q)
+        self.lib.oracle_attention_f16(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), b, s, h, d,
+                                      1 if causal else 0)
+        return O.view(np.float16)
+
+    def attention_f16_rows(self, Q, K, V, causal, b, h, row0, nrows):
+        """Rows [row0, row0 + nrows) of O for batch b, head h: (nrows, dim) fp16."""
+        Q, K, V = _h(Q), _h(K), _h(V)
+        B, s, H, d = Q.shape
+        assert 0 <= b < B and 0 <= h < H and 0 <= row0 and row0 + nrows <= s
+        O = np.zeros_like(Q)
+        self.lib.oracle_attention_f16_rows(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), s, H, d,
+                                           1 if causal else 0, b, h, row0, nrows)
+        return O.view(np.float16)[b, row0:row0 + nrows, h, :].copy()

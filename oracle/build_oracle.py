@@ -8,19 +8,22 @@ import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "gemm_relu_oracle.c")
+ATTENTION_SRC = os.path.join(HERE, "attention_oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
 
-def build(src=SRC, out=LIB, extra_flags=()):
-    """Compile `src` to the shared library `out` and return its path."""
+def build(src=SRC, out=LIB, extra_flags=(), attention_src=ATTENTION_SRC):
+    """Compile the GEMM + ReLU oracle `src` and the attention oracle
+    `attention_src` into the shared library `out`; return its path."""
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
-           "-shared", "-fPIC", *extra_flags, "-o", out, src, "-lm"]
+           "-shared", "-fPIC", *extra_flags, "-o", out, src, attention_src, "-lm"]
     subprocess.run(cmd, check=True)
     return out
 
 
 def needs_build(src=SRC, out=LIB):
-    return (not os.path.exists(out)) or os.path.getmtime(out) < os.path.getmtime(src)
+    return (not os.path.exists(out)) or any(
+        os.path.getmtime(out) < os.path.getmtime(f) for f in (src, ATTENTION_SRC))
 
 
 if __name__ == "__main__":
