@@ -1,0 +1,123 @@
+"""Attention forward on the GPU against the attention oracle (fp64 softmax of
+Q K^T / sqrt(d), times V, one fp16 rounding)."""
+import numpy as np
+import pytest
+
+import tiled_tensor_core_03_gb300 as gr
+
+from gpu_common import dev, host
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 1e-2
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    assert gr.status() == gr.OK
+
+
+def _inputs(b, s, h, d, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return tuple((rng.standard_normal((b, s, h, d)) * sc).astype(np.float16)
+                 for sc in (scale, scale, 1.0))
+
+
+def _check(orc, got, Q, K, V, causal, rows=None):
+    """Contract |g - o| <= atol + rtol |o|, and the bound the method's own
+    rounding allows: P rounded to fp16 (relative 2^-11 per weight), fp32
+    accumulation and the output rounding, i.e.
+        |g - o| <= ulp16(o) + 2^-10 * sum_j w_j |v_j| + 1e-6."""
+    want = orc.attention_f16(Q, K, V, causal).astype(np.float64)
+    absv = orc.attention_f16(Q, K, np.abs(V), causal).astype(np.float64)
+    g = got.astype(np.float64)
+    if rows is not None:
+        want, absv, g = want[rows], absv[rows], g[rows]
+    err = np.abs(g - want)
+    assert np.isfinite(g).all()
+    assert (err <= ATOL + RTOL * np.abs(want)).all(), float(err.max())
+    ulp = np.spacing(np.abs(want).astype(np.float16)).astype(np.float64)
+    bound = ulp + 2.0 ** -10 * absv + 1e-6
+    assert (err <= bound).all(), float((err - bound).max())
+
+
+CASES = [(1, 128, 1, 64, False), (1, 128, 1, 128, True), (2, 200, 3, 64, True),
+         (1, 300, 2, 128, False), (2, 513, 2, 128, True), (1, 1, 1, 64, False),
+         (1, 1, 2, 128, True), (1, 130, 1, 64, False), (3, 384, 2, 64, True),
+         (1, 1000, 2, 128, True), (1, 777, 3, 128, False)]
+
+
+@pytest.mark.parametrize("b,s,h,d,causal", CASES)
+def test_attention_parity(orc, b, s, h, d, causal):
+    import torch
+    Q, K, V = _inputs(b, s, h, d, seed=b * 1000 + s + h + d + int(causal))
+    q, k, v = dev(Q), dev(K), dev(V)
+    out = gr.flash_attention(q, k, v, causal=causal)
+    assert gr.status() == gr.OK
+    _check(orc, host(out), Q, K, V, causal)
+    again = gr.flash_attention(q, k, v, causal=causal)
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))   # fixed order
+
+
+def test_attention_large_scores_and_long_sequence(orc):
+    """Scores of several units (Q, K ~ N(0, 2^2)): the running maximum moves
+    often, exercising the output rescale; two heads, 2048 keys."""
+    Q, K, V = _inputs(1, 2048, 2, 128, seed=9, scale=2.0)
+    out = host(gr.flash_attention(dev(Q), dev(K), dev(V), causal=False))
+    _check(orc, out, Q, K, V, False)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_bench_shape_sampled(orc, causal):
+    """The benchmark's shape (batch 4, 4096 tokens, 32 heads, d = 128):
+    sampled (batch, head, row) triples against the oracle's row entry point."""
+    b, s, h, d = 4, 4096, 32, 128
+    Q, K, V = _inputs(b, s, h, d, seed=11)
+    out = host(gr.flash_attention(dev(Q), dev(K), dev(V), causal=causal))
+    rng = np.random.default_rng(12)
+    for _ in range(12):
+        bb, hh = int(rng.integers(b)), int(rng.integers(h))
+        r0 = int(rng.integers(0, s - 4))
+        want = orc.attention_f16_rows(Q, K, V, causal, bb, hh, r0, 4).astype(np.float64)
+        absv = orc.attention_f16_rows(Q, K, np.abs(V), causal, bb, hh, r0, 4).astype(np.float64)
+        g = out[bb, r0:r0 + 4, hh].astype(np.float64)
+        err = np.abs(g - want)
+        ulp = np.spacing(np.abs(want).astype(np.float16)).astype(np.float64)
+        assert (err <= ATOL + RTOL * np.abs(want)).all()
+        assert (err <= ulp + 2.0 ** -10 * absv + 1e-6).all(), (bb, hh, r0)
+
+
+def test_attention_closed_forms(orc):
+    """K = 0: O is the mean of the visible V rows; causal row 0 is V row 0."""
+    Q, K, V = _inputs(1, 256, 2, 64, seed=13)
+    K[:] = 0
+    out = host(gr.flash_attention(dev(Q), dev(K), dev(V), causal=True))
+    assert np.array_equal(out[:, 0].view(np.uint16), V[:, 0].view(np.uint16))
+    _check(orc, out, Q, K, V, True)
+
+
+def test_attention_rejects_bad_arguments():
+    import torch
+    q = torch.zeros((1, 8, 1, 96), dtype=torch.float16, device="cuda")
+    rc = gr.flash_attention_f16(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), 1, 8, 1,
+                                96, 0, torch.cuda.current_stream().cuda_stream)
+    assert rc == gr.ERR_INVALID_ARG
+    assert gr.flash_attention_f16(0, 0, 0, 0, 0, 8, 1, 64, 0, None) == gr.OK
+
+
+def test_attention_dropped_arrival_times_out_and_recovers(orc):
+    Q, K, V = _inputs(1, 512, 2, 128, seed=14)
+    q, k, v = dev(Q), dev(K), dev(V)
+    gr.gemm_relu_debug_set(1, 20_000_000)
+    try:
+        gr.flash_attention(q, k, v, causal=True)
+        assert gr.status() == gr.ERR_TIMEOUT
+    finally:
+        gr.gemm_relu_debug_set(0, 0)
+    out = host(gr.flash_attention(q, k, v, causal=True))
+    assert gr.status() == gr.OK
+    _check(orc, out, Q, K, V, True)

@@ -71,6 +71,8 @@ def lib():
         L.gemm_relu_debug_force_kernel.restype = i32
         L.gemm_relu_debug_force_split.argtypes = [i32]
         L.gemm_relu_debug_force_split.restype = i32
+        L.flash_attention_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i32, vp]
+        L.flash_attention_f16.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
         L.gemm_relu_debug_set.restype = i32
         _lib = L
@@ -105,6 +107,11 @@ def gemm_relu_f16_splitk_noalloc(A, B, C, M, N, K, split_k, stream=None):
     """Split-K without a caller workspace, for callers that may not allocate
     device memory; uses the library's fixed 8 MiB device scratch array."""
     return lib().gemm_relu_f16_splitk_noalloc(A, B, C, M, N, K, split_k, stream)
+
+
+def flash_attention_f16(Q, K, V, O, batch, seq, heads, head_dim, causal, stream=None):
+    return lib().flash_attention_f16(Q, K, V, O, batch, seq, heads, head_dim, int(causal),
+                                     stream)
 
 
 def gemm_relu_status(stream=None):
@@ -246,3 +253,22 @@ def gemm_relu_splitk(a, b, split_k, out=None, workspace=None, stream=None):
 def status(stream=None):
     """Synchronise and return (and clear) the device watchdog status."""
     return gemm_relu_status(_stream_ptr(stream))
+
+
+def flash_attention(q, k, v, causal=False, out=None, stream=None):
+    """O = softmax(q k^T / sqrt(d)) v for fp16 CUDA tensors shaped
+    [batch, seq, heads, d] (d = 64 or 128), causal or not."""
+    import torch
+    for t in (q, k, v):
+        if t.dtype != torch.float16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-D float16 CUDA tensors [b, s, h, d]")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k and v must have the same shape")
+    if out is None:
+        out = torch.empty_like(q)
+    b, s, h, d = q.shape
+    rc = flash_attention_f16(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), b, s, h, d,
+                             causal, _stream_ptr(stream))
+    if rc != OK:
+        raise GemmReluError(rc, "flash_attention_f16")
+    return out

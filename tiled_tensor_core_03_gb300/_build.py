@@ -8,8 +8,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = [os.path.join(CSRC, "gemm_relu_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_relu_kernels.cuh", "gemm_relu_splitk.cuh", "gemm_relu_2sm.cuh", "gemm_relu_gemv.cuh", "sm103.cuh")] + [
-    os.path.join(INCLUDE, "gemm_relu.h")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_relu_kernels.cuh", "gemm_relu_splitk.cuh", "gemm_relu_2sm.cuh", "gemm_relu_gemv.cuh", "flash_attention.cuh", "sm103.cuh")] + [
+    os.path.join(INCLUDE, "gemm_relu.h"), os.path.join(INCLUDE, "flash_attention.h")]
 LIB = os.path.join(PKG, "libgemmrelu.so")
 
 NVCC_FLAGS = [

@@ -1,0 +1,383 @@
+// flash_attention.cuh -- attention forward, O = softmax(Q K^T / sqrt(d)) V,
+// for fp16 Q, K, V, O in the [batch][seq][heads][dim] layout, fp32 inside.
+//
+// The FlashAttention section of the TileLang tutorial pages: never form the
+// seq x seq scores; stream K/V blocks and keep, per query row, a running
+// maximum m, a running denominator l and an unnormalised output, rescaling
+// the output by 2^(m_old - m_new) when the maximum grows; exponentials in
+// base 2 with alpha = log2(e) / sqrt(d) folded into the scores; only P, the
+// matrix fed to the second product, is rounded to fp16; causal mode stops at
+// the diagonal block and masks its strictly upper triangle.
+//
+// On sm_103a one CTA owns a 128-row query tile of one (batch, head):
+//   warp 0      TMA: the Q tile once, then K and V blocks of 128 keys into a
+//               2-stage ring (4-D tensor maps over the bshd layout, 64-wide
+//               128-byte-swizzled boxes);
+//   warp 1      one thread issues tcgen05.mma: S_j = Q K_j^T into one of two
+//               TMEM score buffers, then O += P_{j-1} V_{j-1} into the TMEM
+//               output accumulator;
+//   warps 2..5  one thread per query row (its TMEM lane): row maximum, base-2
+//               exponentials, row sum, P as fp16 into a K-major swizzled
+//               shared tile (the A operand of the second product), the output
+//               rescale in TMEM when the maximum grew, and at the end O / l,
+//               rounded to fp16 and stored.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "gemm_relu_kernels.cuh"
+
+namespace gemmrelu {
+namespace attn {
+
+constexpr int BM = 128;          // query rows per CTA (UMMA M, TMEM lanes)
+constexpr int BN = 128;          // keys per block
+constexpr int UKA = 16;          // K of one tcgen05.mma kind::f16
+constexpr int kKV = 2;           // K/V ring stages
+constexpr int kThreads = 192;
+constexpr int kSoftWarp0 = 2;
+constexpr uint32_t kSub = BM * 128;   // one [128 rows][64] fp16 swizzled sub-tile: 16 KB
+
+template <int HD>
+struct Cfg {
+    static_assert(HD == 64 || HD == 128, "head dim 64 or 128");
+    static constexpr int kDSub = HD / 64;
+    static constexpr uint32_t kQBytes = kDSub * kSub;   // [128 q][HD]: K-major sub-tiles
+    static constexpr uint32_t kKBytes = kDSub * kSub;   // [128 keys][HD]: K-major sub-tiles
+    static constexpr uint32_t kVBytes = kDSub * kSub;   // [128 keys][HD]: N-major 64-wide slabs
+    static constexpr uint32_t kPBytes = 2 * kSub;       // [128 q][128 keys]: K-major sub-tiles
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffK = kOffQ + kQBytes;
+    static constexpr uint32_t kOffV = kOffK + kKV * kKBytes;
+    static constexpr uint32_t kOffP = kOffV + kKV * kVBytes;
+    static constexpr uint32_t kOffBar = kOffP + kPBytes;
+    // q_full, k_full[kKV], v_full[kKV], kv_empty[kKV], s_full[2], s_free[2],
+    // p_full, pv_done, drain
+    static constexpr uint32_t kNumBars = 1 + 3 * kKV + 2 + 2 + 3;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 512;          // S: 2 x 128 columns, O: HD
+    static constexpr uint32_t kTmemO = 2 * BN;
+    // S = Q K^T: both K-major.  O += P V: P K-major, V N-major.
+    static constexpr uint32_t kIdescS = make_idesc_f16_f32(BM, BN, 0, 0);
+    static constexpr uint32_t kIdescO = make_idesc_f16_f32(BM, HD, 0, 1);
+};
+
+struct Params {
+    uint16_t *O;           // [batch][seq][heads][dim] fp16
+    int batch, seq, heads;
+    int q_tiles;           // ceil(seq / BM)
+    int causal;
+    float scale;           // log2(e) / sqrt(dim)
+    int drop_arrive;
+    uint64_t wait_limit_ns;
+};
+
+// Pack two fp32 values as an fp16 pair (round to nearest even), low = a.
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    flash_attention_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                               const __grid_constant__ CUtensorMap tmK,
+                               const __grid_constant__ CUtensorMap tmV, const Params p) {
+    using G = Cfg<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const uint32_t bar0 = base + G::kOffBar;
+    const uint32_t q_full = bar0;
+    auto k_full = [&](uint32_t s) { return bar0 + 8u * (1 + s); };
+    auto v_full = [&](uint32_t s) { return bar0 + 8u * (1 + kKV + s); };
+    auto kv_empty = [&](uint32_t s) { return bar0 + 8u * (1 + 2 * kKV + s); };
+    auto s_full = [&](uint32_t b) { return bar0 + 8u * (1 + 3 * kKV + b); };
+    auto s_free = [&](uint32_t b) { return bar0 + 8u * (3 + 3 * kKV + b); };
+    const uint32_t p_full = bar0 + 8u * (5 + 3 * kKV);
+    const uint32_t pv_done = bar0 + 8u * (6 + 3 * kKV);
+    const uint32_t drain_bar = bar0 + 8u * (7 + 3 * kKV);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + G::kOffMisc);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // heaviest tiles first in causal mode (tile t has t + 1 key blocks)
+    const int tile = p.causal ? (p.q_tiles - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    const int head = blockIdx.y, batch = blockIdx.z;
+    const int q0 = tile * BM;
+    const int kv_blocks_all = (p.seq + BN - 1) / BN;
+    const int nb = p.causal ? (tile + 1 < kv_blocks_all ? tile + 1 : kv_blocks_all) : kv_blocks_all;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1u);
+        for (uint32_t s = 0; s < (uint32_t)kKV; ++s) {
+            mbar_init(k_full(s), 1u);
+            mbar_init(v_full(s), 1u);
+            mbar_init(kv_empty(s), 1u);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1u);
+            mbar_init(s_free(b), 4u);
+        }
+        mbar_init(p_full, 4u);
+        mbar_init(pv_done, 1u);
+        mbar_init(drain_bar, 1u);
+        *abort_flag = 0u;
+        fence_mbar_init();
+        pdl_launch_dependents();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), G::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    pdl_wait_primary();  // the previous grid of the stream has completed
+
+    if (warp == 0) {
+        // ============================================================ TMA producer
+        if (lane == 0) {
+            uint32_t issued = 0, parity = 0;  // K/V stages with copies in flight
+            bool q_issued = false;
+            if (!(p.drop_arrive && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)) {
+                mbar_arrive_expect_tx(q_full, G::kQBytes);
+#pragma unroll
+                for (int d = 0; d < G::kDSub; ++d)
+                    tma_load_4d(&tmQ, base + G::kOffQ + d * kSub, q_full, 64 * d, head, q0, batch);
+                q_issued = true;
+            }
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
+                if (!wait_bounded(kv_empty(st), ph ^ 1u, p.wait_limit_ns, abort_flag,
+                                  kSiteProducerEmpty))
+                    break;
+                mbar_arrive_expect_tx(k_full(st), G::kKBytes);
+#pragma unroll
+                for (int d = 0; d < G::kDSub; ++d)
+                    tma_load_4d(&tmK, base + G::kOffK + st * G::kKBytes + d * kSub, k_full(st),
+                                64 * d, head, j * BN, batch);
+                mbar_arrive_expect_tx(v_full(st), G::kVBytes);
+#pragma unroll
+                for (int d = 0; d < G::kDSub; ++d)
+                    tma_load_4d(&tmV, base + G::kOffV + st * G::kVBytes + d * kSub, v_full(st),
+                                64 * d, head, j * BN, batch);
+                issued |= 1u << st;
+                parity = (parity & ~(1u << st)) | (ph << st);
+            }
+            // every copy issued must have landed before the CTA may exit
+            if (q_issued)
+                wait_drain(q_full, 0u, p.wait_limit_ns, abort_flag);
+            for (uint32_t s = 0; s < (uint32_t)kKV; ++s)
+                if (issued & (1u << s)) {
+                    wait_drain(k_full(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
+                    wait_drain(v_full(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
+                }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            bool ok = wait_bounded(q_full, 0u, p.wait_limit_ns, abort_flag, kSiteMmaFull);
+            const uint32_t q_base = base + G::kOffQ, p_base = base + G::kOffP;
+            // O += P_i V_i (accumulator initialised by i = 0)
+            auto pv = [&](int i) -> bool {
+                const uint32_t st = (uint32_t)(i % kKV), ph = (uint32_t)((i / kKV) & 1);
+                if (!wait_bounded(p_full, (uint32_t)(i & 1), p.wait_limit_ns, abort_flag,
+                                  kSiteMmaAccEmpty) ||
+                    !wait_bounded(v_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t v_base = base + G::kOffV + st * G::kVBytes;
+#pragma unroll
+                for (int kk = 0; kk < BN / UKA; ++kk) {
+                    const uint64_t adesc = make_sdesc_sw128(
+                        p_base + (kk / 4) * kSub + (kk % 4) * (UKA * 2), 16, 1024);
+                    const uint64_t bdesc = make_sdesc_sw128(v_base + kk * (UKA * 128), kSub, 1024);
+                    umma_f16(tmem_base + G::kTmemO, adesc, bdesc, G::kIdescO,
+                             (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(pv_done);
+                umma_commit(kv_empty(st));
+                return true;
+            };
+            for (int j = 0; ok && j < nb; ++j) {
+                const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
+                const uint32_t b = (uint32_t)(j & 1);
+                if (!wait_bounded(k_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull) ||
+                    !wait_bounded(s_free(b), (uint32_t)(((j >> 1) & 1) ^ 1), p.wait_limit_ns,
+                                  abort_flag, kSiteMmaAccEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t k_base = base + G::kOffK + st * G::kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < HD / UKA; ++kk) {
+                    const uint32_t off = (kk / 4) * kSub + (kk % 4) * (UKA * 2);
+                    umma_f16(tmem_base + b * BN, make_sdesc_sw128(q_base + off, 16, 1024),
+                             make_sdesc_sw128(k_base + off, 16, 1024), G::kIdescS,
+                             kk > 0 ? 1u : 0u);
+                }
+                umma_commit(s_full(b));
+                if (j >= 1 && !pv(j - 1))
+                    ok = false;
+            }
+            if (ok)
+                pv(nb - 1);
+            // all MMAs of this thread complete before TMEM can be released
+            umma_commit(drain_bar);
+            wait_drain(drain_bar, 0u, p.wait_limit_ns, abort_flag);
+        }
+    } else {
+        // ============================================================ softmax / output
+        const int q = warp & 3;                        // TMEM lanes 32q .. 32q+31
+        const int r = 32 * q + lane;                   // query row in the tile
+        const int qi = q0 + r;                         // query index in the sequence
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const uint32_t p_base = base + G::kOffP;
+        float m = -INFINITY, l = 0.0f;
+        bool alive = true;
+        for (int j = 0; alive && j < nb; ++j) {
+            const uint32_t b = (uint32_t)(j & 1);
+            const bool ok = wait_bounded(s_full(b), (uint32_t)((j >> 1) & 1), p.wait_limit_ns,
+                                         abort_flag, kSiteEpiAccFull);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after_sync();
+            const uint32_t s_addr = tmem_base + lane_base + b * BN;
+            const bool masked = (j + 1) * BN > p.seq || (p.causal && j == nb - 1);
+            const int key0 = j * BN;
+            auto visible = [&](int c) {
+                const int key = key0 + c;
+                return key < p.seq && !(p.causal && key > qi);
+            };
+            // pass 1: the block's row maximum (scaled scores)
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_x32_sync(s_addr + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = __uint_as_float(v[i]) * p.scale;
+                    if (!masked || visible(c0 + i))
+                        mx = fmaxf(mx, x);
+                }
+            }
+            const float m_new = fmaxf(m, mx);
+            const float alpha = exp2f(m - m_new);      // 0 at the first block
+            // pass 2: exponentials, their sum, and P rounded to fp16
+            uint32_t ph[BN / 2];
+            float sum = 0.0f;
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_x32_sync(s_addr + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float e0 = exp2f(__uint_as_float(v[i]) * p.scale - m_new);
+                    float e1 = exp2f(__uint_as_float(v[i + 1]) * p.scale - m_new);
+                    if (masked) {
+                        if (!visible(c0 + i))
+                            e0 = 0.0f;
+                        if (!visible(c0 + i + 1))
+                            e1 = 0.0f;
+                    }
+                    sum += e0;
+                    sum += e1;
+                    ph[(c0 + i) / 2] = pack_half2(e0, e1);
+                }
+            }
+            l = l * alpha + sum;
+            m = m_new;
+            // the score buffer may be overwritten (S_{j+2})
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(s_free(b));
+            // P and O are free once the previous block's P V has completed
+            if (j >= 1) {
+                const bool done = wait_bounded(pv_done, (uint32_t)((j - 1) & 1), p.wait_limit_ns,
+                                               abort_flag, kSiteEpiAccFull);
+                if (!__all_sync(0xffffffffu, done)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after_sync();
+            }
+#pragma unroll
+            for (int c16 = 0; c16 < BN / 8; ++c16)
+                st_shared_v4(p_base + (uint32_t)(c16 / 8) * kSub +
+                                 sw128_offset((uint32_t)r, (uint32_t)(c16 % 8)),
+                             ph[4 * c16], ph[4 * c16 + 1], ph[4 * c16 + 2], ph[4 * c16 + 3]);
+            // rescale this warp's output rows when any of their maxima grew
+            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t v[32];
+                    const uint32_t o_addr = tmem_base + lane_base + G::kTmemO + c0;
+                    tmem_ld_x32_sync(o_addr, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tmem_st_x32(o_addr, v);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();  // P visible to the tensor cores
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(p_full);
+        }
+        // the last block's P V, then O / l rounded to fp16
+        if (alive) {
+            const bool done = wait_bounded(pv_done, (uint32_t)((nb - 1) & 1), p.wait_limit_ns,
+                                           abort_flag, kSiteEpiAccFull);
+            if (__all_sync(0xffffffffu, done)) {
+                tc_fence_after_sync();
+                const float inv_l = 1.0f / l;
+                uint16_t *dst = p.O + (((int64_t)batch * p.seq + qi) * p.heads + head) * HD;
+#pragma unroll 1
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld_x32_sync(tmem_base + lane_base + G::kTmemO + c0, v);
+                    uint32_t h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        h[i] = pack_half2(__uint_as_float(v[2 * i]) * inv_l,
+                                          __uint_as_float(v[2 * i + 1]) * inv_l);
+                    if (qi < p.seq) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, G::kTmemCols);
+    }
+}
+
+}  // namespace attn
+}  // namespace gemmrelu

@@ -12,15 +12,18 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <utility>
 
 #include "gemm_relu.h"
+#include "flash_attention.h"
 #include "gemm_relu_kernels.cuh"
 #include "gemm_relu_splitk.cuh"
 #include "gemm_relu_2sm.cuh"
 #include "gemm_relu_gemv.cuh"
+#include "flash_attention.cuh"
 
 namespace {
 
@@ -66,6 +69,7 @@ struct DeviceState {
     int split_pairs[4] = {};  // max resident CTA pairs of the cluster form, per bms index
     bool attr_pair = false;
     bool attr_gemv[4] = {false, false, false, false};
+    bool attr_attn[2] = {false, false};
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -619,6 +623,46 @@ int launch_skinny_split(const void *A, const void *B, void *C, int64_t M, int64_
     }
 }
 
+// ---------------------------------------------------------------- attention forward
+namespace FA = gemmrelu::attn;
+
+// [batch][seq][heads][d] fp16 as a 4-D tensor (d innermost), boxes of 64 d x
+// 1 head x 128 rows x 1 batch, 128-byte swizzle, zero fill outside.
+bool make_bshd_map(CUtensorMap *map, const void *ptr, int64_t batch, int64_t seq, int64_t heads,
+                   int64_t d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)seq, (cuuint64_t)batch};
+    cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)(heads * d) * 2,
+                             (cuuint64_t)(seq * heads * d) * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)FA::BM, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+int launch_attention(const CUtensorMap &mQ, const CUtensorMap &mK, const CUtensorMap &mV,
+                     const FA::Params &p, cudaStream_t stream, bool &attr_done) {
+    using G = FA::Cfg<HD>;
+    auto kern = FA::flash_attention_fwd_kernel<HD>;
+    if (!ensure_smem_attr(attr_done, kern, G::kSmemBytes))
+        return GEMMRELU_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)p.q_tiles, (unsigned)p.heads, (unsigned)p.batch);
+    cfg.blockDim = dim3(FA::kThreads);
+    cfg.dynamicSmemBytes = G::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = GEMMRELU_PDL ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return launch_status(cudaLaunchKernelEx(&cfg, kern, mQ, mK, mV, p));
+}
+
 // ---------------------------------------------------------------- no-alloc scratch
 // Split-K scratch for gemm_relu_f16_splitk_noalloc: a fixed array in every
 // device's copy of this module, so callers that cannot allocate still get a
@@ -770,6 +814,41 @@ int gemm_relu_f16_splitk_noalloc(const void *A, const void *B, void *C, int64_t 
     }
     return gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, scratch,
                                 need > 0 ? GEMMRELU_NOALLOC_SCRATCH_BYTES : 0, stream);
+}
+
+int flash_attention_f16(const void *Q, const void *K, const void *V, void *O, int64_t batch,
+                        int64_t seq, int64_t heads, int64_t head_dim, int causal, void *stream) {
+    if (batch < 0 || seq < 0 || heads < 0 || batch > 65535 || heads > 65535 || seq > kMaxDim ||
+        (head_dim != 64 && head_dim != 128))
+        return GEMMRELU_ERR_INVALID_ARG;
+    if (batch == 0 || seq == 0 || heads == 0)
+        return GEMMRELU_OK;
+    if (!Q || !K || !V || !O || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) ||
+        !aligned(O, 16) || batch * seq * heads * head_dim > ((int64_t)1 << 40))
+        return GEMMRELU_ERR_INVALID_ARG;
+    DeviceState *ds = nullptr;
+    int rc = current_device_state(&ds);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    CUtensorMap mQ, mK, mV;
+    if (!make_bshd_map(&mQ, Q, batch, seq, heads, head_dim) ||
+        !make_bshd_map(&mK, K, batch, seq, heads, head_dim) ||
+        !make_bshd_map(&mV, V, batch, seq, heads, head_dim))
+        return GEMMRELU_ERR_LAUNCH;
+    FA::Params p{};
+    p.O = static_cast<uint16_t *>(O);
+    p.batch = (int)batch;
+    p.seq = (int)seq;
+    p.heads = (int)heads;
+    p.q_tiles = (int)((seq + FA::BM - 1) / FA::BM);
+    p.causal = causal ? 1 : 0;
+    p.scale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));  // log2(e) / sqrt(d)
+    p.drop_arrive = g_drop_arrive.load();
+    p.wait_limit_ns = wait_limit_ns();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (head_dim == 64)
+        return launch_attention<64>(mQ, mK, mV, p, s, ds->attr_attn[0]);
+    return launch_attention<128>(mQ, mK, mV, p, s, ds->attr_attn[1]);
 }
 
 int gemm_relu_status(void *stream) {

@@ -72,6 +72,18 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap *map, uint32_t dst
         : "memory");
 }
 
+// 4-D tiled load global -> shared (c0 innermost), completion counted in bytes
+// on `bar`.
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap *map, uint32_t dst, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3)
+        : "memory");
+}
+
 // L2 policy for data read once: its lines are the first to be replaced, so a
 // stream does not push other (for instance dirty) lines out of L2.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
