@@ -572,6 +572,180 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+# ------------------------------------------------------------------ attention forward
+
+ATTN_SHAPES = {"attn": (4, 4096, 32, 128, False), "attn_causal": (4, 4096, 32, 128, True)}
+
+
+def attn_flops(b, s, h, d, causal):
+    """2 d multiply-adds for Q K^T and 2 d for P V per visible (query, key) pair."""
+    pairs = s * (s + 1) // 2 if causal else s * s
+    return 4 * b * h * d * pairs
+
+
+def run_attention(args, world, rank, local):
+    """Attention forward (flash_attention_f16) on [batch, seq, heads, d] fp16:
+    K launches back to back on rotating input copies, events at both ends."""
+    import multiprocessing
+    import torch
+    import tiled_tensor_core_03_gb300 as gr
+    from tiled_tensor_core_03_gb300 import _build
+
+    if _build.needs_build():
+        _build.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    b, s, h, d, causal = ATTN_SHAPES[args.workload]
+    rng = np.random.default_rng(6)
+    host = [rng.standard_normal((b, s, h, d), dtype=np.float32).astype(np.float16) for _ in range(3)]
+    sets = [[torch.from_numpy(x).to(device) for x in host] + [torch.empty((b, s, h, d), dtype=torch.float16, device=device)]
+            for _ in range(INPUT_SETS)]
+    stream = torch.cuda.current_stream(device)
+
+    def launch(r):
+        q, k, v, o = sets[r]
+        gr.flash_attention(q, k, v, causal=causal, out=o, stream=stream)
+
+    for i in range(args.warmup):
+        launch(i % INPUT_SETS)
+    torch.cuda.synchronize(device)
+    if gr.status(stream) != gr.OK:
+        raise RuntimeError("device status after warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    sampler.mark("t_start")
+    e0.record(stream)
+    for i in range(args.steps):
+        launch(i % INPUT_SETS)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    sampler.mark("t_end")
+    barrier(world)
+    sampler.stop()
+    if gr.status(stream) != gr.OK:
+        raise RuntimeError("device status after timed steps")
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+    flops = attn_flops(b, s, h, d, causal)
+    value = world * flops / (ms * 1e-3) / 1e12
+    # cold single launches after an L2 flush
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    clean = torch.ones(L2_CLEAN_BYTES, dtype=torch.uint8, device=device)
+    cold = []
+    for i in range(max(3, args.steps // 5)):
+        flush.zero_()
+        torch.amax(clean)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        launch(0)
+        c1.record(stream)
+        torch.cuda.synchronize(device)
+        cold.append(c0.elapsed_time(c1))
+    # end to end: inputs from pinned host memory, the output back
+    pinned = [torch.from_numpy(x).pin_memory() for x in host]
+    hout = torch.empty((b, s, h, d), dtype=torch.float16).pin_memory()
+
+    def e2e_step():
+        q, k, v, o = sets[0]
+        for dst, src in zip((q, k, v), pinned):
+            dst.copy_(src, non_blocking=True)
+        gr.flash_attention(q, k, v, causal=causal, out=o, stream=stream)
+        hout.copy_(o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    x0 = torch.cuda.Event(enable_timing=True)
+    x1 = torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, world, device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    peaks, peaks_src = load_peaks()
+    peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP16_PER_BF16
+    peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP16_PER_BF16
+    name = f"{args.workload} (batch {b}, seq {s}, heads {h}, d {d}, {'causal' if causal else 'non-causal'}, bshd fp16, N(0,1))"
+    line = {
+        "metric": "attention forward TFLOP/s (fp16 in, fp32 acc)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": name, "flops_per_step": flops, "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2: {INPUT_SETS} rotating copies of Q, K, V "
+                         f"({3 * b * s * h * d * 2 / 2**20:.0f} MiB each set)",
+                   "timing": "launches back to back, CUDA events at the two ends"},
+        "roofline": {"bound": "tensor", "kernel": f"flash_attention_fwd_kernel<{d}>",
+                     "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / world / peak, "frac_of_sustained": value / world / peak_sus,
+                     "ms": ms, "algorithmic_flops": flops,
+                     "peak_source": f"{peaks_src} bf16_tflops (burst) x {FP16_PER_BF16} (fp16/bf16)",
+                     "traffic": None},
+        "cold_launch": {"ms": statistics.mean(cold),
+                        "tflops": flops / (statistics.mean(cold) * 1e-3) / 1e12},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * b * s * h * d * 2,
+                "d2h_bytes_per_step": b * s * h * d * 2,
+                "api": "tiled_tensor_core_03_gb300.flash_attention from pinned host buffers"},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.Oracle()
+        Q, K, V = host
+        lock = threading.Lock()
+        state = {"next": 0, "flops": 0}
+        rows_out = {}
+        t0 = time.perf_counter()
+        threads = os.cpu_count() or 1
+
+        def worker():
+            while True:
+                with lock:
+                    if time.perf_counter() - t0 >= args.cpu_budget and state["next"] > 0:
+                        return
+                    idx = state["next"]
+                    state["next"] += 1
+                bb, hh, r = (idx // s) % b, (idx // (s * b)) % h, idx % s
+                out = orc.attention_f16_rows(Q, K, V, causal, bb, hh, r, 1)
+                with lock:
+                    state["flops"] += 4 * d * ((r + 1) if causal else s)
+                    rows_out[(bb, hh, r)] = out
+        pool = [threading.Thread(target=worker) for _ in range(threads)]
+        for t in pool:
+            t.start()
+        for t in pool:
+            t.join()
+        dt = time.perf_counter() - t0
+        got = sets[0][3].cpu().numpy()
+        err = max(float(np.abs(got[bb, r, hh].astype(np.float64) - o[0].astype(np.float64)).max())
+                  for (bb, hh, r), o in rows_out.items())
+        line["cpu_baseline"] = {
+            "value": state["flops"] / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows_out)} output rows of the workload ({state['flops'] / 1e9:.2f} GFLOP "
+                      f"in {dt:.1f} s of wall time), fp64 C oracle on {threads} threads; host has "
+                      f"{multiprocessing.cpu_count()} cores",
+            "max_abs_err_vs_gpu_on_sample": err,
+        }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,7 +757,7 @@ def main(argv=None):
                     help="seconds of wall time for the cpu_baseline sample")
     ap.add_argument("--workload", default="step",
                     choices=["step", "square256", "square1024", "ragged", "square4096", "skinny",
-                             "decode1"])
+                             "decode1", "attn", "attn_causal"])
     ap.add_argument("--shape", default=None, help="MxNxK: one custom fused (or split) GEMM")
     ap.add_argument("--split", type=int, default=1, help="split-K for --shape")
     ap.add_argument("--no-streamk", action="store_true",
@@ -591,6 +765,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     world, rank, local = dist_env()
+    if args.workload in ATTN_SHAPES:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "GEMM + ReLU oracle; attention is measured by --impl ours only"}))
+            return 0
+        return run_attention(args, world, rank, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_ours(args, world, rank, local)

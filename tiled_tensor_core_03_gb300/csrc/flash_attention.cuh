@@ -74,6 +74,21 @@ struct Params {
     uint64_t wait_limit_ns;
 };
 
+// 2^x by the hardware's base-2 exponential (approximate, relative error near
+// 2^-22; flushes subnormal results to zero) -- ample for P, which is then
+// rounded to fp16.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The running maximum used as the exponent reference moves (and the output
+// is rescaled) only when a row's maximum exceeds it by more than this many
+// units of log2: P then stays below 2^8, well inside fp16, and the
+// normalisation by the same reference keeps the result exact up to rounding.
+constexpr float kRescaleLog2 = 8.0f;
+
 // Pack two fp32 values as an fp16 pair (round to nearest even), low = a.
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
@@ -256,51 +271,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after_sync();
             const uint32_t s_addr = tmem_base + lane_base + b * BN;
-            const bool masked = (j + 1) * BN > p.seq || (p.causal && j == nb - 1);
-            const int key0 = j * BN;
-            auto visible = [&](int c) {
-                const int key = key0 + c;
-                return key < p.seq && !(p.causal && key > qi);
-            };
-            // pass 1: the block's row maximum (scaled scores)
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_x32_sync(s_addr + c0, v);
+            // the row's 128 raw scores, one TMEM read
+            uint32_t sv[BN];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = __uint_as_float(v[i]) * p.scale;
-                    if (!masked || visible(c0 + i))
-                        mx = fmaxf(mx, x);
-                }
+            for (int c0 = 0; c0 < BN; c0 += 32)
+                tmem_ld_x32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[c0]));
+            tmem_ld_wait();
+            if ((j + 1) * BN > p.seq || (p.causal && j == nb - 1)) {
+                // keys past the sequence, and (causal) keys after the query
+                const int kmax = p.causal ? (qi + 1 < p.seq ? qi + 1 : p.seq) : p.seq;
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    sv[c] = (j * BN + c < kmax) ? sv[c] : __float_as_uint(-INFINITY);
             }
-            const float m_new = fmaxf(m, mx);
-            const float alpha = exp2f(m - m_new);      // 0 at the first block
-            // pass 2: exponentials, their sum, and P rounded to fp16
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; c += 2) {
+                mx0 = fmaxf(mx0, __uint_as_float(sv[c]));
+                mx1 = fmaxf(mx1, __uint_as_float(sv[c + 1]));
+            }
+            const float m_blk = fmaxf(mx0, mx1) * p.scale;   // scale > 0
+            // move the reference only when the maximum grew by more than
+            // kRescaleLog2 (always at the first block)
+            const bool move = m_blk > m + kRescaleLog2;
+            const float m_ref = move ? m_blk : m;
+            const float alpha = move ? fast_exp2(m - m_ref) : 1.0f;   // 0 at the first block
+            float sum0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f, sum3 = 0.0f;
             uint32_t ph[BN / 2];
-            float sum = 0.0f;
 #pragma unroll
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_x32_sync(s_addr + c0, v);
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float e0 = exp2f(__uint_as_float(v[i]) * p.scale - m_new);
-                    float e1 = exp2f(__uint_as_float(v[i + 1]) * p.scale - m_new);
-                    if (masked) {
-                        if (!visible(c0 + i))
-                            e0 = 0.0f;
-                        if (!visible(c0 + i + 1))
-                            e1 = 0.0f;
-                    }
-                    sum += e0;
-                    sum += e1;
-                    ph[(c0 + i) / 2] = pack_half2(e0, e1);
-                }
+            for (int c = 0; c < BN; c += 4) {
+                const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), p.scale, -m_ref));
+                const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), p.scale, -m_ref));
+                const float e2 = fast_exp2(fmaf(__uint_as_float(sv[c + 2]), p.scale, -m_ref));
+                const float e3 = fast_exp2(fmaf(__uint_as_float(sv[c + 3]), p.scale, -m_ref));
+                sum0 += e0;
+                sum1 += e1;
+                sum2 += e2;
+                sum3 += e3;
+                ph[c / 2] = pack_half2(e0, e1);
+                ph[c / 2 + 1] = pack_half2(e2, e3);
             }
-            l = l * alpha + sum;
-            m = m_new;
+            l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+            m = m_ref;
             // the score buffer may be overwritten (S_{j+2})
             tc_fence_before_sync();
             __syncwarp();
@@ -321,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st_shared_v4(p_base + (uint32_t)(c16 / 8) * kSub +
                                  sw128_offset((uint32_t)r, (uint32_t)(c16 % 8)),
                              ph[4 * c16], ph[4 * c16 + 1], ph[4 * c16 + 2], ph[4 * c16 + 3]);
-            // rescale this warp's output rows when any of their maxima grew
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+            // rescale this warp's output rows when any of their references moved
+            if (j >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t v[32];
