@@ -599,6 +599,8 @@ def run_attention(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     b, s, h, d, causal = ATTN_SHAPES[args.workload]
+    if args.attn_shape:
+        b, s, h, d = (int(x) for x in args.attn_shape.split(","))
     rng = np.random.default_rng(6)
     host = [rng.standard_normal((b, s, h, d), dtype=np.float32).astype(np.float16) for _ in range(3)]
     sets = [[torch.from_numpy(x).to(device) for x in host] + [torch.empty((b, s, h, d), dtype=torch.float16, device=device)]
@@ -760,6 +762,8 @@ def main(argv=None):
                              "decode1", "attn", "attn_causal"])
     ap.add_argument("--shape", default=None, help="MxNxK: one custom fused (or split) GEMM")
     ap.add_argument("--split", type=int, default=1, help="split-K for --shape")
+    ap.add_argument("--attn-shape", default=None,
+                    help="batch,seq,heads,d for --workload attn / attn_causal")
     ap.add_argument("--no-streamk", action="store_true",
                     help="time the plain data-parallel fused kernel instead of the stream-K call")
     args = ap.parse_args(argv)
