@@ -4,23 +4,26 @@
 // The FlashAttention section of the TileLang tutorial pages: never form the
 // seq x seq scores; stream K/V blocks and keep, per query row, a running
 // maximum m, a running denominator l and an unnormalised output, rescaling
-// the output by 2^(m_old - m_new) when the maximum grows; exponentials in
+// the output by 2^(m_old - m_new) when the maximum moves; exponentials in
 // base 2 with alpha = log2(e) / sqrt(d) folded into the scores; only P, the
 // matrix fed to the second product, is rounded to fp16; causal mode stops at
 // the diagonal block and masks its strictly upper triangle.
 //
-// On sm_103a one CTA owns a 128-row query tile of one (batch, head):
-//   warp 0      TMA: the Q tile once, then K and V blocks of 128 keys into a
-//               2-stage ring (4-D tensor maps over the bshd layout, 64-wide
+// On sm_103a one CTA owns two 128-row query tiles (t = 0, 1) of one
+// (batch, head) and ping-pongs them so that the tensor core works on one
+// tile while the other's softmax runs:
+//   warps 0-3   softmax of tile 0, one thread per query row (its TMEM lane);
+//   warps 4-7   softmax of tile 1;
+//   warp 8      TMA: both Q tiles once, then K and V blocks of 128 keys into
+//               a 2-stage ring (4-D tensor maps over the bshd layout, 64-wide
 //               128-byte-swizzled boxes);
-//   warp 1      one thread issues tcgen05.mma: S_j = Q K_j^T into one of two
-//               TMEM score buffers, then O += P_{j-1} V_{j-1} into the TMEM
-//               output accumulator;
-//   warps 2..5  one thread per query row (its TMEM lane): row maximum, base-2
-//               exponentials, row sum, P as fp16 into a K-major swizzled
-//               shared tile (the A operand of the second product), the output
-//               rescale in TMEM when the maximum grew, and at the end O / l,
-//               rounded to fp16 and stored.
+//   warp 9      one thread issues tcgen05.mma in the order
+//                 S0_0, S1_0, { PV0_j, S0_j+1, PV1_j, S1_j+1 } for j = 0, 1, ...
+//               with S_t = Q_t K_j^T in TMEM and O_t += P_t V_j, P_t read
+//               from TMEM (the softmax writes it over the scores it has read).
+// TMEM columns: S0 / P0 at 0, S1 / P1 at 128, O0 at 256, O1 at 256 + d.
+// A score MMA for tile t is issued only after the P V MMA that reads P_t,
+// and tcgen05 operations of one thread execute in issue order.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -31,12 +34,14 @@
 namespace gemmrelu {
 namespace attn {
 
-constexpr int BM = 128;          // query rows per CTA (UMMA M, TMEM lanes)
+constexpr int BM = 128;          // query rows per tile (UMMA M, TMEM lanes)
 constexpr int BN = 128;          // keys per block
 constexpr int UKA = 16;          // K of one tcgen05.mma kind::f16
 constexpr int kKV = 2;           // K/V ring stages
-constexpr int kThreads = 192;
-constexpr int kSoftWarp0 = 2;
+constexpr int kTiles = 2;        // query tiles per CTA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr uint32_t kSub = BM * 128;   // one [128 rows][64] fp16 swizzled sub-tile: 16 KB
 
 template <int HD>
@@ -46,20 +51,19 @@ struct Cfg {
     static constexpr uint32_t kQBytes = kDSub * kSub;   // [128 q][HD]: K-major sub-tiles
     static constexpr uint32_t kKBytes = kDSub * kSub;   // [128 keys][HD]: K-major sub-tiles
     static constexpr uint32_t kVBytes = kDSub * kSub;   // [128 keys][HD]: N-major 64-wide slabs
-    static constexpr uint32_t kPBytes = 2 * kSub;       // [128 q][128 keys]: K-major sub-tiles
-    static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffK = kOffQ + kQBytes;
+    static constexpr uint32_t kOffQ = 0;                // + t * kQBytes
+    static constexpr uint32_t kOffK = kOffQ + kTiles * kQBytes;
     static constexpr uint32_t kOffV = kOffK + kKV * kKBytes;
-    static constexpr uint32_t kOffP = kOffV + kKV * kVBytes;
-    static constexpr uint32_t kOffBar = kOffP + kPBytes;
-    // q_full, k_full[kKV], v_full[kKV], kv_empty[kKV], s_full[2], s_free[2],
-    // p_full, pv_done, drain
-    static constexpr uint32_t kNumBars = 1 + 3 * kKV + 2 + 2 + 3;
+    static constexpr uint32_t kOffBar = kOffV + kKV * kVBytes;
+    // q_full, k_full[kKV], v_full[kKV], kv_empty[kKV], s_full[2], p_full[2],
+    // o_full, drain
+    static constexpr uint32_t kNumBars = 1 + 3 * kKV + 2 + 2 + 2;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
-    static constexpr uint32_t kTmemCols = 512;          // S: 2 x 128 columns, O: HD
-    static constexpr uint32_t kTmemO = 2 * BN;
-    // S = Q K^T: both K-major.  O += P V: P K-major, V N-major.
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmemS = 0;               // + t * BN
+    static constexpr uint32_t kTmemO = 2 * BN;          // + t * HD
+    // S = Q K^T: both K-major.  O += P V: P from TMEM (K-major), V N-major.
     static constexpr uint32_t kIdescS = make_idesc_f16_f32(BM, BN, 0, 0);
     static constexpr uint32_t kIdescO = make_idesc_f16_f32(BM, HD, 0, 1);
 };
@@ -68,6 +72,7 @@ struct Params {
     uint16_t *O;           // [batch][seq][heads][dim] fp16
     int batch, seq, heads;
     int q_tiles;           // ceil(seq / BM)
+    int ctas_x;            // ceil(q_tiles / 2)
     int causal;
     float scale;           // log2(e) / sqrt(dim)
     int drop_arrive;
@@ -111,22 +116,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto k_full = [&](uint32_t s) { return bar0 + 8u * (1 + s); };
     auto v_full = [&](uint32_t s) { return bar0 + 8u * (1 + kKV + s); };
     auto kv_empty = [&](uint32_t s) { return bar0 + 8u * (1 + 2 * kKV + s); };
-    auto s_full = [&](uint32_t b) { return bar0 + 8u * (1 + 3 * kKV + b); };
-    auto s_free = [&](uint32_t b) { return bar0 + 8u * (3 + 3 * kKV + b); };
-    const uint32_t p_full = bar0 + 8u * (5 + 3 * kKV);
-    const uint32_t pv_done = bar0 + 8u * (6 + 3 * kKV);
-    const uint32_t drain_bar = bar0 + 8u * (7 + 3 * kKV);
+    auto s_full = [&](uint32_t t) { return bar0 + 8u * (1 + 3 * kKV + t); };
+    auto p_full = [&](uint32_t t) { return bar0 + 8u * (3 + 3 * kKV + t); };
+    const uint32_t o_full = bar0 + 8u * (5 + 3 * kKV);
+    const uint32_t drain_bar = bar0 + 8u * (6 + 3 * kKV);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + G::kOffMisc);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + G::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // heaviest tiles first in causal mode (tile t has t + 1 key blocks)
-    const int tile = p.causal ? (p.q_tiles - 1 - (int)blockIdx.x) : (int)blockIdx.x;
+    // heaviest tile pairs first in causal mode
+    const int pair = p.causal ? (p.ctas_x - 1 - (int)blockIdx.x) : (int)blockIdx.x;
     const int head = blockIdx.y, batch = blockIdx.z;
-    const int q0 = tile * BM;
-    const int kv_blocks_all = (p.seq + BN - 1) / BN;
-    const int nb = p.causal ? (tile + 1 < kv_blocks_all ? tile + 1 : kv_blocks_all) : kv_blocks_all;
+    const int kv_all = (p.seq + BN - 1) / BN;
+    // tiles 2 * pair and 2 * pair + 1; their numbers of key blocks
+    const int tile0 = kTiles * pair, tile1 = tile0 + 1;
+    auto blocks_of = [&](int tl) { return p.causal ? (tl + 1 < kv_all ? tl + 1 : kv_all) : kv_all; };
+    const int nb0 = blocks_of(tile0);
+    const int nb1 = tile1 < p.q_tiles ? blocks_of(tile1) : nb0;  // a padding tile: rows not stored
+    const int nb = nb1 > nb0 ? nb1 : nb0;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1u);
@@ -135,23 +143,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(v_full(s), 1u);
             mbar_init(kv_empty(s), 1u);
         }
-        for (uint32_t b = 0; b < 2; ++b) {
-            mbar_init(s_full(b), 1u);
-            mbar_init(s_free(b), 4u);
+        for (uint32_t t = 0; t < (uint32_t)kTiles; ++t) {
+            mbar_init(s_full(t), 1u);
+            mbar_init(p_full(t), 4u);
         }
-        mbar_init(p_full, 4u);
-        mbar_init(pv_done, 1u);
+        mbar_init(o_full, 1u);
         mbar_init(drain_bar, 1u);
         *abort_flag = 0u;
         fence_mbar_init();
         pdl_launch_dependents();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
         tma_prefetch_map(&tmV);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), G::kTmemCols);
         tmem_relinquish();
     }
@@ -161,16 +168,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     pdl_wait_primary();  // the previous grid of the stream has completed
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ============================================================ TMA producer
         if (lane == 0) {
             uint32_t issued = 0, parity = 0;  // K/V stages with copies in flight
             bool q_issued = false;
             if (!(p.drop_arrive && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)) {
-                mbar_arrive_expect_tx(q_full, G::kQBytes);
+                mbar_arrive_expect_tx(q_full, kTiles * G::kQBytes);
+                for (int t = 0; t < kTiles; ++t)
 #pragma unroll
-                for (int d = 0; d < G::kDSub; ++d)
-                    tma_load_4d(&tmQ, base + G::kOffQ + d * kSub, q_full, 64 * d, head, q0, batch);
+                    for (int d = 0; d < G::kDSub; ++d)
+                        tma_load_4d(&tmQ, base + G::kOffQ + t * G::kQBytes + d * kSub, q_full,
+                                    64 * d, head, (tile0 + t) * BM, batch);
                 q_issued = true;
             }
             for (int j = 0; j < nb; ++j) {
@@ -200,95 +209,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_drain(v_full(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
                 }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             bool ok = wait_bounded(q_full, 0u, p.wait_limit_ns, abort_flag, kSiteMmaFull);
-            const uint32_t q_base = base + G::kOffQ, p_base = base + G::kOffP;
-            // O += P_i V_i (accumulator initialised by i = 0)
-            auto pv = [&](int i) -> bool {
-                const uint32_t st = (uint32_t)(i % kKV), ph = (uint32_t)((i / kKV) & 1);
-                if (!wait_bounded(p_full, (uint32_t)(i & 1), p.wait_limit_ns, abort_flag,
+            // S_t = Q_t K_j^T
+            auto score = [&](int t, int j) -> bool {
+                const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
+                if (!wait_bounded(k_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t q_base = base + G::kOffQ + t * G::kQBytes;
+                const uint32_t k_base = base + G::kOffK + st * G::kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < HD / UKA; ++kk) {
+                    const uint32_t off = (kk / 4) * kSub + (kk % 4) * (UKA * 2);
+                    umma_f16(tmem_base + G::kTmemS + t * BN, make_sdesc_sw128(q_base + off, 16, 1024),
+                             make_sdesc_sw128(k_base + off, 16, 1024), G::kIdescS,
+                             kk > 0 ? 1u : 0u);
+                }
+                umma_commit(s_full(t));
+                return true;
+            };
+            // O_t += P_t V_j, P_t from TMEM (over S_t)
+            auto pv = [&](int t, int j) -> bool {
+                const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
+                if (!wait_bounded(p_full(t), (uint32_t)(j & 1), p.wait_limit_ns, abort_flag,
                                   kSiteMmaAccEmpty) ||
                     !wait_bounded(v_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
                     return false;
                 tc_fence_after_sync();
                 const uint32_t v_base = base + G::kOffV + st * G::kVBytes;
 #pragma unroll
-                for (int kk = 0; kk < BN / UKA; ++kk) {
-                    const uint64_t adesc = make_sdesc_sw128(
-                        p_base + (kk / 4) * kSub + (kk % 4) * (UKA * 2), 16, 1024);
-                    const uint64_t bdesc = make_sdesc_sw128(v_base + kk * (UKA * 128), kSub, 1024);
-                    umma_f16(tmem_base + G::kTmemO, adesc, bdesc, G::kIdescO,
-                             (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(pv_done);
-                umma_commit(kv_empty(st));
+                for (int kk = 0; kk < BN / UKA; ++kk)
+                    umma_f16_ts(tmem_base + G::kTmemO + t * HD,
+                                tmem_base + G::kTmemS + t * BN + kk * (UKA / 2),
+                                make_sdesc_sw128(v_base + kk * (UKA * 128), kSub, 1024), G::kIdescO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
+            if (ok)
+                ok = score(0, 0) && score(1, 0);
             for (int j = 0; ok && j < nb; ++j) {
-                const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
-                const uint32_t b = (uint32_t)(j & 1);
-                if (!wait_bounded(k_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull) ||
-                    !wait_bounded(s_free(b), (uint32_t)(((j >> 1) & 1) ^ 1), p.wait_limit_ns,
-                                  abort_flag, kSiteMmaAccEmpty)) {
-                    ok = false;
+                if (j < nb0) {
+                    ok = pv(0, j) && (j + 1 >= nb0 || score(0, j + 1));
+                    if (!ok)
+                        break;
+                }
+                ok = pv(1, j);
+                if (!ok)
                     break;
-                }
-                tc_fence_after_sync();
-                const uint32_t k_base = base + G::kOffK + st * G::kKBytes;
-#pragma unroll
-                for (int kk = 0; kk < HD / UKA; ++kk) {
-                    const uint32_t off = (kk / 4) * kSub + (kk % 4) * (UKA * 2);
-                    umma_f16(tmem_base + b * BN, make_sdesc_sw128(q_base + off, 16, 1024),
-                             make_sdesc_sw128(k_base + off, 16, 1024), G::kIdescS,
-                             kk > 0 ? 1u : 0u);
-                }
-                umma_commit(s_full(b));
-                if (j >= 1 && !pv(j - 1))
-                    ok = false;
+                umma_commit(kv_empty((uint32_t)(j % kKV)));
+                if (j + 1 < nb1)
+                    ok = score(1, j + 1);
             }
             if (ok)
-                pv(nb - 1);
+                umma_commit(o_full);
             // all MMAs of this thread complete before TMEM can be released
             umma_commit(drain_bar);
             wait_drain(drain_bar, 0u, p.wait_limit_ns, abort_flag);
         }
     } else {
         // ============================================================ softmax / output
-        const int q = warp & 3;                        // TMEM lanes 32q .. 32q+31
-        const int r = 32 * q + lane;                   // query row in the tile
-        const int qi = q0 + r;                         // query index in the sequence
+        const int t = warp >> 2;                        // query tile
+        const int q = warp & 3;                         // TMEM lanes 32q .. 32q+31
+        const int r = 32 * q + lane;                    // query row in the tile
+        const int qi = (tile0 + t) * BM + r;            // query index in the sequence
+        const int my_nb = t == 0 ? nb0 : nb1;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const uint32_t p_base = base + G::kOffP;
+        const uint32_t s_addr = tmem_base + lane_base + G::kTmemS + t * BN;
+        const uint32_t o_addr = tmem_base + lane_base + G::kTmemO + t * HD;
+        const int kmax = p.causal ? (qi + 1 < p.seq ? qi + 1 : p.seq) : p.seq;
         float m = -INFINITY, l = 0.0f;
         bool alive = true;
-        for (int j = 0; alive && j < nb; ++j) {
-            const uint32_t b = (uint32_t)(j & 1);
-            const bool ok = wait_bounded(s_full(b), (uint32_t)((j >> 1) & 1), p.wait_limit_ns,
+        for (int j = 0; j < my_nb; ++j) {
+            const bool ok = wait_bounded(s_full((uint32_t)t), (uint32_t)(j & 1), p.wait_limit_ns,
                                          abort_flag, kSiteEpiAccFull);
-            if (!__all_sync(0xffffffffu, ok))
+            if (!__all_sync(0xffffffffu, ok)) {
+                alive = false;
                 break;
+            }
             tc_fence_after_sync();
-            const uint32_t s_addr = tmem_base + lane_base + b * BN;
-            // the row's 128 raw scores, one TMEM read
-            uint32_t sv[BN];
+            // keys past the sequence, and (causal) keys after the query
+            const bool masked = (j + 1) * BN > p.seq || (p.causal && j == my_nb - 1);
+            const int key0 = j * BN;
+            // the row's 128 scores: one TMEM round trip, kept in registers
+            uint32_t v[BN];
 #pragma unroll
             for (int c0 = 0; c0 < BN; c0 += 32)
-                tmem_ld_x32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[c0]));
-            tmem_ld_wait();
-            if ((j + 1) * BN > p.seq || (p.causal && j == nb - 1)) {
-                // keys past the sequence, and (causal) keys after the query
-                const int kmax = p.causal ? (qi + 1 < p.seq ? qi + 1 : p.seq) : p.seq;
+                tmem_ld_x32(s_addr + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    sv[c] = (j * BN + c < kmax) ? sv[c] : __float_as_uint(-INFINITY);
+            for (int c0 = 0; c0 < BN; c0 += 32)
+                tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&v[c0]));
+            if (masked) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                    v[i] = key0 + i < kmax ? v[i] : __float_as_uint(-INFINITY);
             }
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                mx0 = fmaxf(mx0, __uint_as_float(sv[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(sv[c + 1]));
+            for (int i = 0; i < BN; i += 2) {
+                mx0 = fmaxf(mx0, __uint_as_float(v[i]));
+                mx1 = fmaxf(mx1, __uint_as_float(v[i + 1]));
             }
             const float m_blk = fmaxf(mx0, mx1) * p.scale;   // scale > 0
             // move the reference only when the maximum grew by more than
@@ -296,67 +318,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool move = m_blk > m + kRescaleLog2;
             const float m_ref = move ? m_blk : m;
             const float alpha = move ? fast_exp2(m - m_ref) : 1.0f;   // 0 at the first block
+            // exponentials (masked scores are -inf: 2^-inf = 0), their sum,
+            // and P as fp16 over the scores
             float sum0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f, sum3 = 0.0f;
-            uint32_t ph[BN / 2];
 #pragma unroll
-            for (int c = 0; c < BN; c += 4) {
-                const float e0 = fast_exp2(fmaf(__uint_as_float(sv[c]), p.scale, -m_ref));
-                const float e1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), p.scale, -m_ref));
-                const float e2 = fast_exp2(fmaf(__uint_as_float(sv[c + 2]), p.scale, -m_ref));
-                const float e3 = fast_exp2(fmaf(__uint_as_float(sv[c + 3]), p.scale, -m_ref));
-                sum0 += e0;
-                sum1 += e1;
-                sum2 += e2;
-                sum3 += e3;
-                ph[c / 2] = pack_half2(e0, e1);
-                ph[c / 2 + 1] = pack_half2(e2, e3);
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t ph[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[c0 + i]), p.scale, -m_ref));
+                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[c0 + i + 1]), p.scale, -m_ref));
+                    const float e2 = fast_exp2(fmaf(__uint_as_float(v[c0 + i + 2]), p.scale, -m_ref));
+                    const float e3 = fast_exp2(fmaf(__uint_as_float(v[c0 + i + 3]), p.scale, -m_ref));
+                    sum0 += e0;
+                    sum1 += e1;
+                    sum2 += e2;
+                    sum3 += e3;
+                    ph[i / 2] = pack_half2(e0, e1);
+                    ph[i / 2 + 1] = pack_half2(e2, e3);
+                }
+                tmem_st_x16(s_addr + c0 / 2, ph);
             }
             l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
             m = m_ref;
-            // the score buffer may be overwritten (S_{j+2})
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(s_free(b));
-            // P and O are free once the previous block's P V has completed
-            if (j >= 1) {
-                const bool done = wait_bounded(pv_done, (uint32_t)((j - 1) & 1), p.wait_limit_ns,
-                                               abort_flag, kSiteEpiAccFull);
-                if (!__all_sync(0xffffffffu, done)) {
-                    alive = false;
-                    break;
-                }
-                tc_fence_after_sync();
-            }
-#pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16)
-                st_shared_v4(p_base + (uint32_t)(c16 / 8) * kSub +
-                                 sw128_offset((uint32_t)r, (uint32_t)(c16 % 8)),
-                             ph[4 * c16], ph[4 * c16 + 1], ph[4 * c16 + 2], ph[4 * c16 + 3]);
             // rescale this warp's output rows when any of their references moved
+            // (the previous P V of this tile completed before S_j was written)
             if (j >= 1 && __any_sync(0xffffffffu, move)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t v[32];
-                    const uint32_t o_addr = tmem_base + lane_base + G::kTmemO + c0;
-                    tmem_ld_x32_sync(o_addr, v);
+                    tmem_ld_x32_sync(o_addr + c0, v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st_x32(o_addr, v);
+                    tmem_st_x32(o_addr + c0, v);
                 }
-                tmem_st_wait();
             }
-            fence_proxy_async_smem();  // P visible to the tensor cores
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(p_full);
+                mbar_arrive(p_full((uint32_t)t));
         }
-        // the last block's P V, then O / l rounded to fp16
+        // the last P V of both tiles, then O / l rounded to fp16
         if (alive) {
-            const bool done = wait_bounded(pv_done, (uint32_t)((nb - 1) & 1), p.wait_limit_ns,
-                                           abort_flag, kSiteEpiAccFull);
+            const bool done = wait_bounded(o_full, 0u, p.wait_limit_ns, abort_flag,
+                                           kSiteEpiAccFull);
             if (__all_sync(0xffffffffu, done)) {
                 tc_fence_after_sync();
                 const float inv_l = 1.0f / l;
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t v[32];
-                    tmem_ld_x32_sync(tmem_base + lane_base + G::kTmemO + c0, v);
+                    tmem_ld_x32_sync(o_addr + c0, v);
                     uint32_t h[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -385,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, G::kTmemCols);
     }

@@ -651,7 +651,7 @@ int launch_attention(const CUtensorMap &mQ, const CUtensorMap &mK, const CUtenso
     if (!ensure_smem_attr(attr_done, kern, G::kSmemBytes))
         return GEMMRELU_ERR_LAUNCH;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)p.q_tiles, (unsigned)p.heads, (unsigned)p.batch);
+    cfg.gridDim = dim3((unsigned)p.ctas_x, (unsigned)p.heads, (unsigned)p.batch);
     cfg.blockDim = dim3(FA::kThreads);
     cfg.dynamicSmemBytes = G::kSmemBytes;
     cfg.stream = stream;
@@ -841,6 +841,7 @@ int flash_attention_f16(const void *Q, const void *K, const void *V, void *O, in
     p.seq = (int)seq;
     p.heads = (int)heads;
     p.q_tiles = (int)((seq + FA::BM - 1) / FA::BM);
+    p.ctas_x = (p.q_tiles + FA::kTiles - 1) / FA::kTiles;
     p.causal = causal ? 1 : 0;
     p.scale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));  // log2(e) / sqrt(d)
     p.drop_arrive = g_drop_arrive.load();
