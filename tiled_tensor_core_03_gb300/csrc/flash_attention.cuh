@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int j = 0; j < nb; ++j) {
                 const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
-                if (!wait_bounded(kv_empty(st), ph ^ 1u, p.wait_limit_ns, abort_flag,
+                if (!wait_bounded_eager(kv_empty(st), ph ^ 1u, p.wait_limit_ns, abort_flag,
                                   kSiteProducerEmpty))
                     break;
                 mbar_arrive_expect_tx(k_full(st), G::kKBytes);
@@ -212,21 +212,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            bool ok = wait_bounded(q_full, 0u, p.wait_limit_ns, abort_flag, kSiteMmaFull);
+            bool ok = wait_bounded_eager(q_full, 0u, p.wait_limit_ns, abort_flag, kSiteMmaFull);
             // S_t = Q_t K_j^T
             auto score = [&](int t, int j) -> bool {
                 const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
-                if (!wait_bounded(k_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
+                if (!wait_bounded_eager(k_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
                     return false;
                 tc_fence_after_sync();
-                const uint32_t q_base = base + G::kOffQ + t * G::kQBytes;
-                const uint32_t k_base = base + G::kOffK + st * G::kKBytes;
+                // descriptors built once, advanced in their 16-byte units:
+                // 32 bytes per 16 k inside a 64-wide sub-tile, kSub across
+                const uint64_t qd = make_sdesc_sw128(base + G::kOffQ + t * G::kQBytes, 16, 1024);
+                const uint64_t kd = make_sdesc_sw128(base + G::kOffK + st * G::kKBytes, 16, 1024);
+                const uint32_t d_s = tmem_base + G::kTmemS + t * BN;
 #pragma unroll
                 for (int kk = 0; kk < HD / UKA; ++kk) {
-                    const uint32_t off = (kk / 4) * kSub + (kk % 4) * (UKA * 2);
-                    umma_f16(tmem_base + G::kTmemS + t * BN, make_sdesc_sw128(q_base + off, 16, 1024),
-                             make_sdesc_sw128(k_base + off, 16, 1024), G::kIdescS,
-                             kk > 0 ? 1u : 0u);
+                    const uint64_t off = (uint64_t)((kk / 4) * (kSub >> 4) + (kk % 4) * 2);
+                    umma_f16(d_s, qd + off, kd + off, G::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(s_full(t));
                 return true;
@@ -234,18 +235,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_t += P_t V_j, P_t from TMEM (over S_t)
             auto pv = [&](int t, int j) -> bool {
                 const uint32_t st = (uint32_t)(j % kKV), ph = (uint32_t)((j / kKV) & 1);
-                if (!wait_bounded(p_full(t), (uint32_t)(j & 1), p.wait_limit_ns, abort_flag,
+                if (!wait_bounded_eager(p_full(t), (uint32_t)(j & 1), p.wait_limit_ns, abort_flag,
                                   kSiteMmaAccEmpty) ||
-                    !wait_bounded(v_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
+                    !wait_bounded_eager(v_full(st), ph, p.wait_limit_ns, abort_flag, kSiteMmaFull))
                     return false;
                 tc_fence_after_sync();
-                const uint32_t v_base = base + G::kOffV + st * G::kVBytes;
+                // V descriptor advanced 16 key rows (2 KB) per step; P columns 8
+                const uint64_t vd = make_sdesc_sw128(base + G::kOffV + st * G::kVBytes, kSub, 1024);
+                const uint32_t d_o = tmem_base + G::kTmemO + t * HD;
+                const uint32_t a_p = tmem_base + G::kTmemS + t * BN;
 #pragma unroll
                 for (int kk = 0; kk < BN / UKA; ++kk)
-                    umma_f16_ts(tmem_base + G::kTmemO + t * HD,
-                                tmem_base + G::kTmemS + t * BN + kk * (UKA / 2),
-                                make_sdesc_sw128(v_base + kk * (UKA * 128), kSub, 1024), G::kIdescO,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(d_o, a_p + kk * (UKA / 2), vd + (uint64_t)(kk * ((UKA * 128) >> 4)),
+                                G::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
             if (ok)
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m = -INFINITY, l = 0.0f;
         bool alive = true;
         for (int j = 0; j < my_nb; ++j) {
-            const bool ok = wait_bounded(s_full((uint32_t)t), (uint32_t)(j & 1), p.wait_limit_ns,
+            const bool ok = wait_bounded_eager(s_full((uint32_t)t), (uint32_t)(j & 1), p.wait_limit_ns,
                                          abort_flag, kSiteEpiAccFull);
             if (!__all_sync(0xffffffffu, ok)) {
                 alive = false;
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the last P V of both tiles, then O / l rounded to fp16
         if (alive) {
-            const bool done = wait_bounded(o_full, 0u, p.wait_limit_ns, abort_flag,
+            const bool done = wait_bounded_eager(o_full, 0u, p.wait_limit_ns, abort_flag,
                                            kSiteEpiAccFull);
             if (__all_sync(0xffffffffu, done)) {
                 tc_fence_after_sync();

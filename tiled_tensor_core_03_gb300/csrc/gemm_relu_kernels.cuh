@@ -80,6 +80,28 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     }
 }
 
+// wait_bounded without the suspend hint (mbar_try_wait_eager): for the
+// softmax <-> MMA hand-offs of the attention kernel, where the waiting
+// thread's wake-up latency is on the critical path (measured: 5% there).
+__device__ __forceinline__ bool wait_bounded_eager(uint32_t bar, uint32_t parity,
+                                                   uint64_t limit_ns,
+                                                   volatile uint32_t *abort_flag,
+                                                   unsigned where) {
+    if (mbar_try_wait_eager(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_eager(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout(abort_flag, where);
+            return false;
+        }
+    }
+}
+
 // wait_bounded for a phase completed by other CTAs of the cluster (acquire
 // at cluster scope, so their shared-memory writes before arriving are seen).
 __device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,

@@ -353,6 +353,20 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
 
 // Same as mbar_try_wait, with acquire at cluster scope: for phases completed
 // by arrivals (and preceding shared-memory writes) of other CTAs.
+// mbar_try_wait without a suspend-time hint (the instruction's own, short,
+// suspension): for hand-offs whose wake-up latency is on the critical path.
+__device__ __forceinline__ bool mbar_try_wait_eager(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
 #if GEMMRELU_WAIT_HINT_NS > 0
