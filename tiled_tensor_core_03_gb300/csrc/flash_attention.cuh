@@ -322,26 +322,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha = move ? fast_exp2(m - m_ref) : 1.0f;   // 0 at the first block
             // exponentials (masked scores are -inf: 2^-inf = 0), their sum,
             // and P as fp16 over the scores
-            float sum0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f, sum3 = 0.0f;
+            // (pairs of fp32 lanes per instruction: __ffma2_rn / __fadd2_rn
+            // round each lane as fmaf / + would)
+            const float2 sc2 = make_float2(p.scale, p.scale), nm2 = make_float2(-m_ref, -m_ref);
+            float2 sa = make_float2(0.0f, 0.0f), sb = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t ph[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    const float e0 = fast_exp2(fmaf(__uint_as_float(v[c0 + i]), p.scale, -m_ref));
-                    const float e1 = fast_exp2(fmaf(__uint_as_float(v[c0 + i + 1]), p.scale, -m_ref));
-                    const float e2 = fast_exp2(fmaf(__uint_as_float(v[c0 + i + 2]), p.scale, -m_ref));
-                    const float e3 = fast_exp2(fmaf(__uint_as_float(v[c0 + i + 3]), p.scale, -m_ref));
-                    sum0 += e0;
-                    sum1 += e1;
-                    sum2 += e2;
-                    sum3 += e3;
-                    ph[i / 2] = pack_half2(e0, e1);
-                    ph[i / 2 + 1] = pack_half2(e2, e3);
+                    const float2 x01 = __ffma2_rn(
+                        make_float2(__uint_as_float(v[c0 + i]), __uint_as_float(v[c0 + i + 1])), sc2, nm2);
+                    const float2 x23 = __ffma2_rn(
+                        make_float2(__uint_as_float(v[c0 + i + 2]), __uint_as_float(v[c0 + i + 3])), sc2, nm2);
+                    const float2 e01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
+                    const float2 e23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
+                    sa = __fadd2_rn(sa, e01);
+                    sb = __fadd2_rn(sb, e23);
+                    ph[i / 2] = pack_half2(e01.x, e01.y);
+                    ph[i / 2 + 1] = pack_half2(e23.x, e23.y);
                 }
                 tmem_st_x16(s_addr + c0 / 2, ph);
             }
-            l = l * alpha + ((sum0 + sum1) + (sum2 + sum3));
+            l = l * alpha + ((sa.x + sa.y) + (sb.x + sb.y));
             m = m_ref;
             // rescale this warp's output rows when any of their references moved
             // (the previous P V of this tile completed before S_j was written)
