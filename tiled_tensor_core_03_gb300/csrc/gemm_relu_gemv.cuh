@@ -32,6 +32,11 @@
 
 #include "gemm_relu_kernels.cuh"
 
+// Stages each CTA asks L2 to fetch before it waits for the previous grid.
+#ifndef GEMMRELU_GEMV_PREFETCH
+#define GEMMRELU_GEMV_PREFETCH 8
+#endif
+
 namespace gemmrelu {
 namespace gemv {
 
@@ -124,6 +129,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         pdl_launch_dependents();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        // L2 fetches the first stages while the previous grid finishes (L2
+        // is the point of coherence: this moves nothing past the dependence)
+        for (int j = s0; j < s1 && j < s0 + GEMMRELU_GEMV_PREFETCH; ++j) {
+            tma_prefetch_2d(&tmB, n0, j * kRows);
+            tma_prefetch_2d(&tmA, j * kRows, 0);
+        }
     }
     __syncthreads();
     pdl_wait_primary();  // the previous grid of the stream has completed

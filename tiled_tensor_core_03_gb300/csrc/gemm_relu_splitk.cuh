@@ -36,6 +36,11 @@ namespace splitk {
 #ifndef GEMMRELU_SPLIT_KBS
 #define GEMMRELU_SPLIT_KBS 4
 #endif
+// Stages of B (and A) each CTA asks L2 to fetch before it waits for the
+// previous grid; 0 turns it off.
+#ifndef GEMMRELU_SPLIT_PREFETCH
+#define GEMMRELU_SPLIT_PREFETCH 4
+#endif
 
 constexpr int BNT = 128;     // N per tile (UMMA M, TMEM lanes)
 constexpr int BK = 64;       // one 128-byte swizzle row of fp16
@@ -167,7 +172,6 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_arrive(1, 192);
         if constexpr (kCluster)
             cluster_arrive();
-        pdl_wait_primary();  // the previous grid's writes (A, B) are visible
     } else {
         if (warp == 1) {
             tmem_alloc(smem_addr(tmem_slot), tmem_cols);
@@ -211,6 +215,25 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0) {
         // ============================================================ TMA producer
         if (lane == 0) {
+            // While the previous grid finishes, have L2 fetch the first
+            // stages of this CTA's first unit: the launch-boundary gap in
+            // the HBM stream then overlaps the previous grid's tail.
+            if (GEMMRELU_SPLIT_PREFETCH > 0 && u_first < p.num_units) {
+                int64_t s, nt, mt;
+                int sb0, sb1;
+                unit_coords(u_first, s, nt, mt, sb0, sb1);
+                const int n0 = (int)(nt * BNT), m0 = (int)(mt * BMS);
+                const int sb_end = min(sb1, sb0 + GEMMRELU_SPLIT_PREFETCH);
+                for (int sb = sb0; sb < sb_end; ++sb) {
+                    const int k0 = sb * G::kSuperK;
+                    tma_prefetch_2d(&tmB, n0, k0);
+                    tma_prefetch_2d(&tmB, n0 + 64, k0);
+#pragma unroll
+                    for (int i = 0; i < G::kKbs; ++i)
+                        tma_prefetch_2d(&tmA, k0 + i * BK, m0);
+                }
+            }
+            pdl_wait_primary();  // the previous grid's writes (A, B) are visible
             uint32_t stage = 0, phase = 0, parity = 0, issued = 0;
             bool ok = true;
             // B is read exactly once: stream it through L2 as evict-first

@@ -79,6 +79,15 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Warm L2 with one 2-D box of a tensor (no shared memory, no barrier).  L2 is
+// the device's point of coherence, so this may run before the previous grid's
+// writes are visible: it moves nothing past the data dependence.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // 2-D tiled load global -> shared, completion counted in bytes on `bar`.
 // c0 is the innermost (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap *map, uint32_t dst, uint32_t bar,
