@@ -43,10 +43,12 @@ METRIC = "GEMM+ReLU TFLOP/s (fp16 in, fp32 acc)"
 # kernels, keyed by (kind, M, N, K); a shape missing here reports null.
 DRAM_BYTES_PER_LAUNCH = {
     # profiles/dram_traffic_bench_launches.md, first captured launch of each:
-    # pair kernel with stream-K at 4096^3: 76,848,896 B read + 27,169,536 B written
-    ("streamk", 4096, 4096, 4096): 104018432,
-    # split-K CTA-pair form at 16x8192x8192, split 8: 134,519,552 B read + 88,320 B written
-    ("splitk", 16, 8192, 8192): 134607872,
+    # pair kernel with stream-K at 4096^3: 75,324,416 B read + 26,401,280 B written
+    ("streamk", 4096, 4096, 4096): 101725696,
+    # split-K CTA-pair form at 16x8192x8192, split 8: 134,542,592 B read + 101,120 B written
+    ("splitk", 16, 8192, 8192): 134643712,
+    # GEMV kernel at 1x8192x8192: 134,254,336 B read + 2,791,168 B written
+    ("streamk", 1, 8192, 8192): 137045504,
 }
 
 
