@@ -61,9 +61,11 @@ typedef enum {
  *   - M >= 256 and N >= 256 with TMA-capable A, B, C: 256 x 256 tiles on CTA
  *     pairs (tcgen05.mma.cta_group::2), when that needs no more waves than
  *     one CTA per 128 x 256 tile;
- *   - M <= 4 with TMA-capable A and B: the GEMV kernel -- B streamed through
- *     shared memory, fp32 multiply-adds on the CUDA cores, K chunks reduced
- *     in a fixed order inside a thread-block cluster (the GEMV pattern of
+ *   - M <= 2, or M <= 4 unless the case below applies with one CTA pair
+ *     per 128 columns all resident at once (2 * ceil(N / 128) <= SMs), with
+ *     TMA-capable A and B: the GEMV kernel -- B streamed through shared
+ *     memory, fp32 multiply-adds on the CUDA cores, K chunks reduced in a
+ *     fixed order inside a thread-block cluster (the GEMV pattern of
  *     "TileLang CUDA 核心编程模式" section 4);
  *   - M <= 64 with TMA-capable A and B whose 128 x 256 tiles would keep
  *     fewer than half of the SMs busy: gemm_relu_f16_splitk's CTA-pair form

@@ -432,12 +432,15 @@ def test_gemv_integer_inputs_bit_exact(orc, forced_gemv):
 
 
 def test_decode_rows_routing(orc):
-    """gemm_relu_f16 on decode-like rows: M <= 4 runs the GEMV kernel (same
-    bits as forcing it); M = 8 with few column tiles runs K split in two on
-    CTA pairs (same bits as gemm_relu_f16_splitk with split 2); both agree
-    with the oracle and with the tensor-core tile kernel within the bounds."""
+    """gemm_relu_f16 on decode-like rows: M <= 2 runs the GEMV kernel (same
+    bits as forcing it), and so does M = 4 when the CTA pairs of a split
+    would not fit in one wave (N = 16384); M = 4 or 8 with few column tiles
+    runs K split in two on CTA pairs (same bits as gemm_relu_f16_splitk with
+    split 2); all agree with the oracle and with the tensor-core tile kernel
+    within the bounds."""
     import torch
-    for M, N, K in [(4, 4096, 4096), (8, 4096, 4096)]:
+    for M, N, K, route in [(2, 4096, 4096, "gemv"), (4, 16384, 512, "gemv"),
+                           (4, 4096, 4096, "split2"), (8, 4096, 4096, "split2")]:
         A, B = inputs.make(M, N, K, dist="uniform", seed=70 + M)
         a, b = dev(A), dev(B)
         auto = gr.gemm_relu(a, b)
@@ -450,8 +453,8 @@ def test_decode_rows_routing(orc):
             gr.gemm_relu_debug_force_kernel(gr.KERNEL_AUTO)
         split2 = gr.gemm_relu_splitk(a, b, 2)
         assert gr.status() == gr.OK
-        same = gemv if M <= 4 else split2
-        assert torch.equal(auto.view(torch.int16), same.view(torch.int16)), M
+        same = gemv if route == "gemv" else split2
+        assert torch.equal(auto.view(torch.int16), same.view(torch.int16)), (M, N, route)
         want = orc.gemm_relu_f16(A, B)
         for name, got in (("auto", auto), ("gemv", gemv), ("tile", tile), ("split2", split2)):
             assert_parity(host(got), want, abs_dot(A, B), K, (M, name))

@@ -309,11 +309,24 @@ namespace V = gemmrelu::gemv;
 // below is faster (29 us).
 constexpr int64_t kGemvMaxM = 4;
 
-bool use_gemv(const void *A, const void *B, int64_t M, int64_t N, int64_t K) {
+bool use_skinny_split(const void *A, const void *B, int64_t M, int64_t N, int64_t K, int sms);
+
+// Decode-like rows.  M <= 2: the GEMV kernel.  M = 3 or 4: the GEMV kernel's
+// four accumulator rows cost issue slots, and the split-K pair form with
+// S = 2 streams B faster when its pairs (one per 128 columns) fit in one
+// wave (measured 4096^2: 11.3 vs 12.3 us; 8192^2: 22.6 vs 23.5 us); with
+// more columns the GEMV kernel stays ahead (16384^2: 78.6 vs 84.2 us).
+bool use_gemv(const void *A, const void *B, int64_t M, int64_t N, int64_t K, int sms) {
     const int force = g_force_kernel.load();
     if (force != 0 && force != 4)
         return false;
-    return M <= (force == 4 ? (int64_t)V::kMaxM : kGemvMaxM) && tma_ok(A, K) && tma_ok(B, N);
+    if (M > (force == 4 ? (int64_t)V::kMaxM : kGemvMaxM) || !tma_ok(A, K) || !tma_ok(B, N))
+        return false;
+    if (force == 4 || M <= 2)
+        return true;
+    const bool split_one_wave = 2 * ((N + 127) / 128) <= (int64_t)sms &&
+                                use_skinny_split(A, B, M, N, K, sms);
+    return !split_one_wave;
 }
 
 // K chunks per column block (the cluster size): doubled while the grid stays
@@ -380,13 +393,11 @@ bool use_pair(int64_t M, int64_t N, int sms, int path) {
 
 int launch_skinny_split(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                         cudaStream_t stream, DeviceState *ds);
-bool use_skinny_split(const void *A, const void *B, int64_t M, int64_t N, int64_t K, int sms);
-
 int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                  cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
     namespace F = gemmrelu::fused;
     const int path = fused_path(A, B, C, M, N, K);
-    if (sk.dp_tiles < 0 && use_gemv(A, B, M, N, K))
+    if (sk.dp_tiles < 0 && use_gemv(A, B, M, N, K, ds->sms))
         return launch_gemv(A, B, C, M, N, K, stream, ds);
     if (sk.dp_tiles < 0 && use_skinny_split(A, B, M, N, K, ds->sms))
         return launch_skinny_split(A, B, C, M, N, K, stream, ds);
