@@ -577,6 +577,12 @@ def run_ours(args, world, rank, local):
 # ------------------------------------------------------------------ attention forward
 
 ATTN_SHAPES = {"attn": (4, 4096, 32, 128, False), "attn_causal": (4, 4096, 32, 128, True)}
+# profiles/dram_traffic_bench_launches.md, first captured launch of each attention workload
+# (batch, seq, heads, d, causal): DRAM bytes read + written
+ATTN_DRAM_BYTES_PER_LAUNCH = {
+    (4, 4096, 32, 128, False): 402995712 + 113100800,
+    (4, 4096, 32, 128, True): 402901504 + 114983936,
+}
 
 
 def attn_flops(b, s, h, d, causal):
@@ -698,7 +704,7 @@ def run_attention(args, world, rank, local):
                      "frac": value / world / peak, "frac_of_sustained": value / world / peak_sus,
                      "ms": ms, "algorithmic_flops": flops,
                      "peak_source": f"{peaks_src} bf16_tflops (burst) x {FP16_PER_BF16} (fp16/bf16)",
-                     "traffic": None},
+                     "traffic": ATTN_DRAM_BYTES_PER_LAUNCH.get((b, s, h, d, bool(causal)))},
         "cold_launch": {"ms": statistics.mean(cold),
                         "tflops": flops / (statistics.mean(cold) * 1e-3) / 1e12},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
