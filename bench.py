@@ -585,6 +585,98 @@ ATTN_DRAM_BYTES_PER_LAUNCH = {
 }
 
 
+ATTN_METRIC = "attention forward TFLOP/s (fp16 in, fp32 acc)"
+
+
+def attn_workload_name(workload, b, s, h, d, causal):
+    return (f"{workload} (batch {b}, seq {s}, heads {h}, d {d}, "
+            f"{'causal' if causal else 'non-causal'}, bshd fp16, N(0,1))")
+
+
+def attn_shape(args):
+    b, s, h, d, causal = ATTN_SHAPES[args.workload]
+    if args.attn_shape:
+        b, s, h, d = (int(x) for x in args.attn_shape.split(","))
+    return b, s, h, d, causal
+
+
+def attn_host_inputs(b, s, h, d):
+    """Seeded Q, K, V (standard normal, fp16) of the attention workloads."""
+    rng = np.random.default_rng(6)
+    return [rng.standard_normal((b, s, h, d), dtype=np.float32).astype(np.float16) for _ in range(3)]
+
+
+def attn_oracle_sample(Q, K, V, causal, budget_s, threads=None):
+    """The attention oracle as it stands on whole output rows (batch, head,
+    query row), taken in a fixed order by `threads` host threads until
+    `budget_s` of wall time has passed.  Returns (flops, seconds, threads,
+    {(b, h, row): fp16 row})."""
+    import oracle
+    orc = oracle.Oracle()
+    b, s, h, d = Q.shape
+    lock = threading.Lock()
+    state = {"next": 0, "flops": 0}
+    rows_out = {}
+    threads = threads or os.cpu_count() or 1
+    t0 = time.perf_counter()
+
+    def worker():
+        while True:
+            with lock:
+                if time.perf_counter() - t0 >= budget_s and state["next"] > 0:
+                    return
+                idx = state["next"]
+                state["next"] += 1
+            bb, hh, r = (idx // s) % b, (idx // (s * b)) % h, idx % s
+            out = orc.attention_f16_rows(Q, K, V, causal, bb, hh, r, 1)
+            with lock:
+                state["flops"] += 4 * d * ((r + 1) if causal else s)
+                rows_out[(bb, hh, r)] = out
+    pool = [threading.Thread(target=worker) for _ in range(threads)]
+    for t in pool:
+        t.start()
+    for t in pool:
+        t.join()
+    return state["flops"], time.perf_counter() - t0, threads, rows_out
+
+
+def run_reference_attention(args, world, rank):
+    """The reference arm for the attention workloads: the attention oracle as
+    it stands, each step a bounded sample of whole output rows."""
+    if rank != 0:
+        return 0
+    import multiprocessing
+    b, s, h, d, causal = attn_shape(args)
+    Q, K, V = attn_host_inputs(b, s, h, d)
+    budget = min(2.0, 150.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        attn_oracle_sample(Q, K, V, causal, budget * 0.25)
+    flops, secs, threads = 0, 0.0, 1
+    for _ in range(args.steps):
+        f, dt, threads, _ = attn_oracle_sample(Q, K, V, causal, budget)
+        flops += f
+        secs += dt
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference",
+        "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": attn_workload_name(args.workload, b, s, h, d, causal),
+                   "parallelism": f"replicas{args.gpus}"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step, whole output rows (batch, head, query row) for "
+                                   f"about {budget:.2f} s of wall time of the fp64 C attention "
+                                   f"oracle on {threads} threads; host has "
+                                   f"{multiprocessing.cpu_count()} cores"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def attn_flops(b, s, h, d, causal):
     """2 d multiply-adds for Q K^T and 2 d for P V per visible (query, key) pair."""
     pairs = s * (s + 1) // 2 if causal else s * s
@@ -606,11 +698,8 @@ def run_attention(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    b, s, h, d, causal = ATTN_SHAPES[args.workload]
-    if args.attn_shape:
-        b, s, h, d = (int(x) for x in args.attn_shape.split(","))
-    rng = np.random.default_rng(6)
-    host = [rng.standard_normal((b, s, h, d), dtype=np.float32).astype(np.float16) for _ in range(3)]
+    b, s, h, d, causal = attn_shape(args)
+    host = attn_host_inputs(b, s, h, d)
     sets = [[torch.from_numpy(x).to(device) for x in host] + [torch.empty((b, s, h, d), dtype=torch.float16, device=device)]
             for _ in range(INPUT_SETS)]
     stream = torch.cuda.current_stream(device)
@@ -689,9 +778,9 @@ def run_attention(args, world, rank, local):
     peaks, peaks_src = load_peaks()
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP16_PER_BF16
     peak_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP16_PER_BF16
-    name = f"{args.workload} (batch {b}, seq {s}, heads {h}, d {d}, {'causal' if causal else 'non-causal'}, bshd fp16, N(0,1))"
+    name = attn_workload_name(args.workload, b, s, h, d, causal)
     line = {
-        "metric": "attention forward TFLOP/s (fp16 in, fp32 acc)", "value": value, "unit": "TFLOP/s",
+        "metric": ATTN_METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
@@ -715,33 +804,9 @@ def run_attention(args, world, rank, local):
         "clocks": sampler.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        import oracle
-        orc = oracle.Oracle()
         Q, K, V = host
-        lock = threading.Lock()
-        state = {"next": 0, "flops": 0}
-        rows_out = {}
-        t0 = time.perf_counter()
-        threads = os.cpu_count() or 1
-
-        def worker():
-            while True:
-                with lock:
-                    if time.perf_counter() - t0 >= args.cpu_budget and state["next"] > 0:
-                        return
-                    idx = state["next"]
-                    state["next"] += 1
-                bb, hh, r = (idx // s) % b, (idx // (s * b)) % h, idx % s
-                out = orc.attention_f16_rows(Q, K, V, causal, bb, hh, r, 1)
-                with lock:
-                    state["flops"] += 4 * d * ((r + 1) if causal else s)
-                    rows_out[(bb, hh, r)] = out
-        pool = [threading.Thread(target=worker) for _ in range(threads)]
-        for t in pool:
-            t.start()
-        for t in pool:
-            t.join()
-        dt = time.perf_counter() - t0
+        flops_s, dt, threads, rows_out = attn_oracle_sample(Q, K, V, causal, args.cpu_budget)
+        state = {"flops": flops_s}
         got = sets[0][3].cpu().numpy()
         err = max(float(np.abs(got[bb, r, hh].astype(np.float64) - o[0].astype(np.float64)).max())
                   for (bb, hh, r), o in rows_out.items())
@@ -779,9 +844,7 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.workload in ATTN_SHAPES:
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
-                              "GEMM + ReLU oracle; attention is measured by --impl ours only"}))
-            return 0
+            return run_reference_attention(args, world, rank)
         return run_attention(args, world, rank, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
