@@ -297,6 +297,10 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=device)
 
     parts, name = build_parts(args)
+    if args.kernel != "auto":
+        # profiling aid: every GEMM call of this run takes the named kernel
+        gr.gemm_relu_debug_force_kernel(KERNEL_CHOICES[args.kernel])
+        name += f", kernel forced: {args.kernel}"
     host_inputs = {label: inputs.make_workload(w) for label, w, _ in parts}
     # INPUT_SETS device copies of each part's operands (and outputs): the
     # back-to-back timed loop rotates through them, so a launch never finds
@@ -586,6 +590,8 @@ ATTN_DRAM_BYTES_PER_LAUNCH = {
 
 
 ATTN_METRIC = "attention forward TFLOP/s (fp16 in, fp32 acc)"
+# --kernel: the library's debug hook that pins the GEMM kernel (0 = its own choice)
+KERNEL_CHOICES = {"auto": 0, "one_cta_256": 1, "one_cta_128": 2, "pair": 3, "gemv": 4}
 
 
 def attn_workload_name(workload, b, s, h, d, causal):
@@ -837,6 +843,8 @@ def main(argv=None):
     ap.add_argument("--split", type=int, default=1, help="split-K for --shape")
     ap.add_argument("--attn-shape", default=None,
                     help="batch,seq,heads,d for --workload attn / attn_causal")
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_CHOICES),
+                    help="pin the GEMM kernel (a profiling aid; default: the library's choice)")
     ap.add_argument("--no-streamk", action="store_true",
                     help="time the plain data-parallel fused kernel instead of the stream-K call")
     args = ap.parse_args(argv)
