@@ -432,25 +432,55 @@ def run_ours(args, world, rank, local):
         pinned[label] = (torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(),
                          torch.empty((w.M, w.N), dtype=torch.float16).pin_memory())
 
-    def e2e_step():
+    # Uploads run on their own stream, the kernels on `stream`, read-backs on
+    # a third: each step still moves all of its inputs up and its result down
+    # inside the timed region, while the copy engines and the kernels of
+    # neighbouring parts overlap.  Step i uses device set i % INPUT_SETS, and
+    # its upload waits until that set's previous kernel and read-back are done.
+    up_stream = torch.cuda.Stream(device)
+    down_stream = torch.cuda.Stream(device)
+    set_free = {}
+
+    def e2e_step(i):
+        r = i % INPUT_SETS
         for label, w, kind in parts:
             hA, hB, hC = pinned[label]
-            a, b, c, _ = dev[label][0]
-            a.copy_(hA, non_blocking=True)
-            b.copy_(hB, non_blocking=True)
-            launch(label, w, kind)
-            hC.copy_(c, non_blocking=True)
+            a, b, c, _ = dev[label][r]
+            if (label, r) in set_free:
+                up_stream.wait_event(set_free[(label, r)])
+            with torch.cuda.stream(up_stream):
+                a.copy_(hA, non_blocking=True)
+                b.copy_(hB, non_blocking=True)
+            uploaded = torch.cuda.Event()
+            uploaded.record(up_stream)
+            stream.wait_event(uploaded)
+            launch(label, w, kind, r=r)
+            computed = torch.cuda.Event()
+            computed.record(stream)
+            down_stream.wait_event(computed)
+            with torch.cuda.stream(down_stream):
+                hC.copy_(c, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(down_stream)
+            set_free[(label, r)] = done
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_run(n, x0=None, x1=None):
+        if x0 is not None:
+            x0.record(stream)
+            up_stream.wait_event(x0)
+        for i in range(n):
+            e2e_step(i)
+        for ev in set_free.values():          # every read-back inside the region
+            stream.wait_event(ev)
+        if x1 is not None:
+            x1.record(stream)
+
+    e2e_run(args.warmup)
     torch.cuda.synchronize(device)
     barrier(world)
     x0 = torch.cuda.Event(enable_timing=True)
     x1 = torch.cuda.Event(enable_timing=True)
-    x0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    x1.record(stream)
+    e2e_run(args.steps, x0, x1)
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, world, device)
     barrier(world)
@@ -550,7 +580,9 @@ def run_ours(args, world, rank, local):
         "wall_ms_per_step": 1e3 * (wall1 - wall0) / args.steps,
         "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "tiled_tensor_core_03_gb300.gemm_relu_streamk / gemm_relu_splitk from pinned host buffers"},
+                "api": "tiled_tensor_core_03_gb300.gemm_relu_streamk / gemm_relu_splitk from pinned host "
+                       "buffers; uploads, kernels and read-backs on three streams, overlapping "
+                       "across parts and steps"},
         # this library's kernels in the timed region: the fused kernel once,
         # split-K once (CTA-pair form) or twice (partial + reduce)
         "gpu_launches": sum(split_form(w)[1] if kind == "splitk" else 1
@@ -758,22 +790,50 @@ def run_attention(args, world, rank, local):
     pinned = [torch.from_numpy(x).pin_memory() for x in host]
     hout = torch.empty((b, s, h, d), dtype=torch.float16).pin_memory()
 
-    def e2e_step():
-        q, k, v, o = sets[0]
-        for dst, src in zip((q, k, v), pinned):
-            dst.copy_(src, non_blocking=True)
-        gr.flash_attention(q, k, v, causal=causal, out=o, stream=stream)
-        hout.copy_(o, non_blocking=True)
+    # uploads, the kernel and the read-back on three streams (as in the GEMM
+    # bench): step i uses device set i % INPUT_SETS once its previous kernel
+    # and read-back are done
+    up_stream = torch.cuda.Stream(device)
+    down_stream = torch.cuda.Stream(device)
+    set_free = {}
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_step(i):
+        r = i % INPUT_SETS
+        q, k, v, o = sets[r]
+        if r in set_free:
+            up_stream.wait_event(set_free[r])
+        with torch.cuda.stream(up_stream):
+            for dst, src in zip((q, k, v), pinned):
+                dst.copy_(src, non_blocking=True)
+        uploaded = torch.cuda.Event()
+        uploaded.record(up_stream)
+        stream.wait_event(uploaded)
+        gr.flash_attention(q, k, v, causal=causal, out=o, stream=stream)
+        computed = torch.cuda.Event()
+        computed.record(stream)
+        down_stream.wait_event(computed)
+        with torch.cuda.stream(down_stream):
+            hout.copy_(o, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(down_stream)
+        set_free[r] = done
+
+    def e2e_run(n, x0=None, x1=None):
+        if x0 is not None:
+            x0.record(stream)
+            up_stream.wait_event(x0)
+        for i in range(n):
+            e2e_step(i)
+        for ev in set_free.values():
+            stream.wait_event(ev)
+        if x1 is not None:
+            x1.record(stream)
+
+    e2e_run(args.warmup)
     torch.cuda.synchronize(device)
     x0 = torch.cuda.Event(enable_timing=True)
     x1 = torch.cuda.Event(enable_timing=True)
-    x0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    x1.record(stream)
+    e2e_run(args.steps, x0, x1)
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, world, device)
     if world > 1:
@@ -805,7 +865,8 @@ def run_attention(args, world, rank, local):
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * b * s * h * d * 2,
                 "d2h_bytes_per_step": b * s * h * d * 2,
-                "api": "tiled_tensor_core_03_gb300.flash_attention from pinned host buffers"},
+                "api": "tiled_tensor_core_03_gb300.flash_attention from pinned host buffers; uploads, "
+                       "kernel and read-back on three streams, overlapping across steps"},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
     }
