@@ -132,6 +132,29 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows res, res + 8, res + 16, ... of a row-major fp16 matrix rows x cols
+// whose pitch need not be a multiple of 16 bytes, as a 2-D tensor for the
+// predicated-load kernel (see gemmrelu::fused::RowMaps): base = the first
+// such row's start rounded down to 16 bytes, row stride 8 rows (16 * cols
+// bytes), cols + off / 2 elements per row (off = the start's byte offset in
+// its 16-byte block), no swizzle, zero fill outside.  Needs res < rows.
+bool make_row_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int64_t res,
+                  uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const uintptr_t start = reinterpret_cast<uintptr_t>(ptr) + (uintptr_t)(2 * res * cols);
+    const uintptr_t base = start & ~(uintptr_t)15;
+    cuuint64_t dims[2] = {(cuuint64_t)(cols + (int64_t)(start - base) / 2),
+                          (cuuint64_t)((rows - res + 7) / 8)};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 16};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, reinterpret_cast<void *>(base), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- argument checks
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -243,11 +266,11 @@ int fused_bn(int64_t M, int64_t N, int sms) {
 
 template <bool kTma, int kBN>
 int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensorMap &mC,
-                    const gemmrelu::fused::Params &p, cudaStream_t stream, DeviceState *ds,
-                    bool &attr_done) {
+                    const gemmrelu::fused::Params &p, const gemmrelu::fused::MapsFor<kTma> &rm,
+                    cudaStream_t stream, DeviceState *ds, bool &attr_done) {
     namespace F = gemmrelu::fused;
     auto kern = F::gemm_relu_fused_kernel<kTma, kBN>;
-    constexpr uint32_t smem = F::Tile<kBN>::kSmemBytes;
+    constexpr uint32_t smem = F::Tile<kBN, kTma>::kSmemBytes;
     if (!ensure_smem_attr(attr_done, kern, smem))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
@@ -255,7 +278,7 @@ int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensor
     // must be resident at once -- a cooperative launch guarantees that (or
     // fails).
     return launch_kernel(kern, (unsigned)grid, F::Roles<kTma>::kThreads, smem, stream,
-                         p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p);
+                         p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p, rm);
 }
 
 // Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
@@ -411,7 +434,8 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     p.N = (int)N;
     p.K = (int)K;
     p.num_kb = (int)((K + F::BK - 1) / F::BK);
-    const int bn = fused_bn(M, N, ds->sms);
+    // The predicated-load producer is laid out for 128 x 128 tiles.
+    const int bn = path == 1 ? fused_bn(M, N, ds->sms) : 128;
     p.m_tiles = (M + F::BM - 1) / F::BM;
     p.n_tiles = (N + bn - 1) / bn;
     p.num_tiles = p.m_tiles * p.n_tiles;
@@ -430,14 +454,20 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
         (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
          !make_map(&mC, C, M, N, 64, 32)))
         return GEMMRELU_ERR_LAUNCH;
-    if (bn == 256) {
-        if (path == 1)
-            return launch_fused_bn<true, 256>(mA, mB, mC, p, stream, ds, ds->attr_fused[0]);
-        return launch_fused_bn<false, 256>(mA, mB, mC, p, stream, ds, ds->attr_fused[1]);
-    }
+    const F::NoMaps none{};
+    if (bn == 256)
+        return launch_fused_bn<true, 256>(mA, mB, mC, p, none, stream, ds, ds->attr_fused[0]);
     if (path == 1)
-        return launch_fused_bn<true, 128>(mA, mB, mC, p, stream, ds, ds->attr_fused[2]);
-    return launch_fused_bn<false, 128>(mA, mB, mC, p, stream, ds, ds->attr_fused[3]);
+        return launch_fused_bn<true, 128>(mA, mB, mC, p, none, stream, ds, ds->attr_fused[2]);
+    // predicated-load kernel: one tensor map per row residue modulo 8 of A and B
+    F::RowMaps rm;
+    std::memset(&rm, 0, sizeof(rm));
+    for (int r = 0; r < 8; ++r) {
+        if ((r < M && !make_row_map(&rm.a[r], A, M, K, r, F::BK + 8, 16)) ||
+            (r < K && !make_row_map(&rm.b[r], B, K, N, r, F::Tile<128, false>::BN + 8, 8)))
+            return GEMMRELU_ERR_LAUNCH;
+    }
+    return launch_fused_bn<false, 128>(mA, mB, mC, p, rm, stream, ds, ds->attr_fused[3]);
 }
 
 // ---------------------------------------------------------------- stream-K plan

@@ -28,6 +28,7 @@
 
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "sm103.cuh"
 
@@ -69,6 +70,28 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
         return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            record_timeout(abort_flag, where);
+            return false;
+        }
+    }
+}
+
+// wait_bounded with a pause of `sleep_ns` between polls: for waits that last
+// a whole tile (the epilogue's), so that the waiting warps leave issue slots
+// to warps that share their scheduler and do the work.
+__device__ __forceinline__ bool wait_bounded_sleep(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                   volatile uint32_t *abort_flag, unsigned where,
+                                                   unsigned sleep_ns) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity))
             return true;
         if (*abort_flag)
@@ -181,21 +204,54 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t j) {
     return r * 128u + ((j ^ (r & 7u)) << 4);
 }
 
-// Eight fp16 values src[col0 .. col0+7] of one row (zero where col >= limit),
-// packed in a uint4.  Uses one 16-byte load when aligned and fully inside.
-__device__ __forceinline__ uint4 load8_pred(const uint16_t *__restrict__ row, int64_t col0,
-                                            int64_t limit) {
-    const uint16_t *p = row + col0;
-    if (col0 + 8 <= limit && (reinterpret_cast<uintptr_t>(p) & 15u) == 0)
-        return __ldg(reinterpret_cast<const uint4 *>(p));
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = (col0 + 2 * e < limit) ? (uint32_t)__ldg(p + 2 * e) : 0u;
-        const uint32_t hi = (col0 + 2 * e + 1 < limit) ? (uint32_t)__ldg(p + 2 * e + 1) : 0u;
-        w[e] = lo | (hi << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+// ------------------------------------------------------------------ predicated loads
+//
+// Operands whose rows TMA cannot describe as a plain matrix (a row pitch or a
+// base address that is not a multiple of 16 bytes) are staged in two steps.
+// A row segment of 8 * G fp16 starts at some even byte offset `off` inside a
+// 16-byte block and so spans G + 1 aligned 16-byte blocks.  First the aligned
+// blocks come into a raw shared-memory slot by TMA (see RowMaps: rows r and
+// r + 8 start at the same offset modulo 16, because eight rows are 16 * cols
+// bytes, so each residue of the rows modulo 8 is a regular 2-D tensor with a
+// 16-byte-aligned base).  Then a group of G lanes walks along each raw row:
+// lane c reads blocks c and c + 1 and funnel-shifts the 32 bytes by `off` to
+// get the 16 bytes of its chunk, which it stores in the operand layout.  A
+// warp that takes the rows of one residue sees one offset per operand for
+// the whole kernel.
+
+// Byte offset `off` (even, 0..14) of a row segment inside its first 16-byte
+// block, split for window16: word shift by 1, word shift by 2, bit shift.
+struct Shift {
+    bool s1, s2;
+    uint32_t sh;
+};
+
+__device__ __forceinline__ Shift make_shift(uint32_t off) {
+    return Shift{(off & 4u) != 0, (off & 8u) != 0, (off & 3u) * 8u};
+}
+
+// The 16 bytes at byte offset `off` of the 32 bytes v0 || v1: the word offset
+// off / 4 as two selects, the half-word rest as a funnel shift.
+__device__ __forceinline__ uint4 window16(const uint4 &v0, const uint4 &v1, const Shift &f) {
+    const uint32_t t0 = f.s1 ? v0.y : v0.x, t1 = f.s1 ? v0.z : v0.y, t2 = f.s1 ? v0.w : v0.z;
+    const uint32_t t3 = f.s1 ? v1.x : v0.w, t4 = f.s1 ? v1.y : v1.x, t5 = f.s1 ? v1.z : v1.y;
+    const uint32_t t6 = f.s1 ? v1.w : v1.z;
+    const uint32_t x0 = f.s2 ? t2 : t0, x1 = f.s2 ? t3 : t1, x2 = f.s2 ? t4 : t2;
+    const uint32_t x3 = f.s2 ? t5 : t3, x4 = f.s2 ? t6 : t4;
+    return make_uint4(__funnelshift_r(x0, x1, f.sh), __funnelshift_r(x1, x2, f.sh),
+                      __funnelshift_r(x2, x3, f.sh), __funnelshift_r(x3, x4, f.sh));
+}
+
+// Keep the first `nvalid` fp16 values of an 8-value chunk, zero the rest.
+__device__ __forceinline__ uint32_t keep_pair(uint32_t w, int nvalid, int e) {
+    return e >= nvalid ? 0u : (e + 1 >= nvalid ? (w & 0xffffu) : w);
+}
+
+__device__ __forceinline__ uint4 keep_first(uint4 v, int nvalid) {
+    if (nvalid >= 8)
+        return v;
+    return make_uint4(keep_pair(v.x, nvalid, 0), keep_pair(v.y, nvalid, 2),
+                      keep_pair(v.z, nvalid, 4), keep_pair(v.w, nvalid, 6));
 }
 
 // tcgen05.ld of 32 / 16 columns fused with its wait, so that no use of the
@@ -241,23 +297,35 @@ constexpr uint32_t kEpiBuf = 32 * 128;      // 32 rows x 64 fp16, swizzled
 constexpr int kEpiWarps = 4;
 
 // Per tile width BN (UMMA N = TMEM columns per accumulator): 256 or 128.
-// The ring gets as many stages as fit beside 32 KB of epilogue staging.
-template <int kBN>
+// The TMA kernels' ring gets as many stages as fit beside 32 KB of epilogue
+// staging.  The predicated-load kernel (kTma false, BN = 128) keeps two
+// operand stages and, before them, a ring of kRawStages raw stages: the
+// aligned 16-byte blocks of each row segment as TMA brings them (A: 128 rows
+// of 9 blocks, B: 64 k-rows of 17 blocks, grouped by row residue modulo 8),
+// which its producers shift into the operand layout.
+template <int kBN, bool kTma = true>
 struct Tile {
     static constexpr int BN = kBN;
     static constexpr uint32_t kBTile = BK * BN * 2;          // BN / 64 slabs, MN-major
-    static constexpr int kStages = kBN >= 256 ? 4 : 6;
+    static constexpr int kStages = kTma ? (kBN >= 256 ? 4 : 6) : 2;
+    static constexpr int kRawStages = kTma ? 0 : 3;
+    static constexpr uint32_t kRawRowA = (BK / 8 + 1) * 16;  // 144 B
+    static constexpr uint32_t kRawRowB = (BN / 8 + 1) * 16;  // 272 B at BN = 128
+    static constexpr uint32_t kRawB = BM * kRawRowA;         // B rows follow the A rows
+    static constexpr uint32_t kRawStage = kRawB + BK * kRawRowB;
     static constexpr uint32_t kTmemCols = 2 * BN;            // double-buffered accumulator
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + kStages * kATile;
-    static constexpr uint32_t kOffEpi = kOffB + kStages * kBTile;
+    static constexpr uint32_t kOffRaw = kOffB + kStages * kBTile;
+    static constexpr uint32_t kOffEpi = kOffRaw + kRawStages * kRawStage;
     static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
-    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+    static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1 + 8 * kRawStages;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
     static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
     // A: K-major (bit 15 = 0); B: N-major (bit 16 = 1); M = 128, N = BN.
     static constexpr uint32_t kIdesc = make_idesc_f16_f32(BM, BN, 0, 1);
+    static_assert(kOffEpi % 1024 == 0 && kSmemBytes <= 232448, "shared memory layout");
 };
 
 struct Params {
@@ -285,6 +353,22 @@ struct Params {
     uint32_t *sk_flags;    // [G][4]: one flag per epilogue warp (32 rows)
     uint32_t epoch;        // nonzero, distinct per call
 };
+
+// Tensor maps of the predicated-load kernel: for each residue a modulo 8, the
+// rows a, a + 8, a + 16, ... of A (and of B) as a 2-D tensor whose base is the
+// first such row's start rounded down to 16 bytes and whose row stride is 8
+// rows (16 * cols bytes, a multiple of 16 whatever cols is).  Element x of
+// such a tensor row is element x - off / 2 of the matrix row (off = the byte
+// offset of the row start inside its 16-byte block), so a box starting at
+// x = k0 brings the aligned blocks that hold elements k0 .. of every row,
+// with the k (or n) tail and the rows past the end zero-filled.
+struct RowMaps {
+    CUtensorMap a[8];      // box: 72 elements (144 B) x 16 rows
+    CUtensorMap b[8];      // box: 136 elements (272 B) x 8 rows
+};
+struct NoMaps {};
+template <bool kTma>
+using MapsFor = typename std::conditional<kTma, NoMaps, RowMaps>::type;
 
 enum ItemKind : int { kItemFull = 0, kItemPieceOut = 1, kItemPieceIn = 2 };
 
@@ -425,7 +509,7 @@ __device__ __forceinline__ void piece_to_tmem(const float *slot, int row, uint32
 
 template <bool kTma>
 struct Roles {
-    static constexpr int kLoadWarps = kTma ? 1 : 4;
+    static constexpr int kLoadWarps = kTma ? 1 : 8;
     static constexpr int kMmaWarp = kLoadWarps;
     static constexpr int kEpiWarp0 = kLoadWarps + 1;
     static constexpr int kThreads = 32 * (kLoadWarps + 1 + kEpiWarps);
@@ -435,9 +519,10 @@ template <bool kTma, int kBN>
 __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     gemm_relu_fused_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
-                           const __grid_constant__ CUtensorMap tmC, const Params p) {
+                           const __grid_constant__ CUtensorMap tmC, const Params p,
+                           const __grid_constant__ MapsFor<kTma> rm) {
     using R = Roles<kTma>;
-    using T = Tile<kBN>;
+    using T = Tile<kBN, kTma>;
     constexpr int BN = T::BN;
     constexpr int kStages = T::kStages;
     constexpr uint32_t kBTile = T::kBTile, kTmemCols = T::kTmemCols, kIdesc = T::kIdesc;
@@ -462,7 +547,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), kTma ? 1u : 32u * R::kLoadWarps);
+            mbar_init(full_bar(s), kTma ? 1u : (uint32_t)R::kLoadWarps);
             mbar_init(empty_bar(s), 1u);
         }
         for (uint32_t b = 0; b < 2; ++b) {
@@ -470,6 +555,8 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             mbar_init(acce_bar(b), (uint32_t)kEpiWarps);
         }
         mbar_init(drain_bar, 1u);
+        for (int b = 0; b < 8 * T::kRawStages; ++b)
+            mbar_init(drain_bar + 8u * (1u + (uint32_t)b), 1u);
         *abort_flag = 0u;
         fence_mbar_init();
         pdl_launch_dependents();
@@ -532,53 +619,167 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                         wait_drain(full_bar(s), (parity >> s) & 1u, p.wait_limit_ns, abort_flag);
             }
         } else {
-            // Predicated loads for operands TMA cannot describe (row pitches
-            // that are not multiples of 16 bytes).  Same swizzled layout.
-            const int tid = threadIdx.x;  // 0 .. 127
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            const int64_t items = num_items(p, blockIdx.x, gridDim.x);
-            for (int64_t it = 0; ok && it < items; ++it) {
-                int64_t t, mb, nb;
-                int kb0, kb1, kind;
-                item_at(p, blockIdx.x, gridDim.x, it, t, kb0, kb1, kind);
-                tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
-                const int64_t m0 = mb * BM, n0 = nb * BN;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_limit_ns, abort_flag,
-                                      kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const int64_t k0 = (int64_t)kb * BK;
-                    const uint32_t adst = base + kOffA + stage * kATile;
-                    for (int c = tid; c < BM * 8; c += 128) {
-                        const int r = c >> 3, j = c & 7;
-                        const int64_t gm = m0 + r;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (gm < p.M)
-                            v = load8_pred(p.A + gm * p.K, k0 + 8 * j, p.K);
-                        st_shared_v4(adst + sw128_offset(r, j), v.x, v.y, v.z, v.w);
-                    }
-                    const uint32_t bdst = base + kOffB + stage * kBTile;
-                    for (int c = tid; c < BK * (BN / 8); c += 128) {
-                        const int j = c & 7, s = (c >> 3) % (BN / 64), r = (c >> 3) / (BN / 64);
-                        const int64_t gk = k0 + r;
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (gk < p.K)
-                            v = load8_pred(p.B + gk * p.N, n0 + 64 * s + 8 * j, p.N);
-                        st_shared_v4(bdst + s * kBSlab + sw128_offset(r, j), v.x, v.y, v.z, v.w);
-                    }
-                    fence_proxy_async_smem();
-                    const bool drop = p.drop_arrive && blockIdx.x == 0 && it == 0 && kb == kb0;
-                    if (!drop)
-                        mbar_arrive(full_bar(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
+            // Predicated loads for operands TMA cannot describe (see window16
+            // and RowMaps).  Eight warps; warp w handles the rows of residue w
+            // modulo 8 of every stage: A rows w + 8i (i < 16), B k-rows w + 8i
+            // (i < 8).  Its lane 0 loads them into its part of a raw slot with
+            // two TMA boxes, kRawStages - 1 stages ahead; once they have
+            // landed, the warp shifts them into the operand stage: A as four
+            // ops of four rows x 8 lanes (a row's 64 k = 128 bytes), B as four
+            // ops of two rows x 16 lanes (a k-row's 128 n = 256 bytes, both
+            // 64-wide slabs).  Each lane reads the raw blocks c and c + 1 of
+            // its row.  A warp reads only the raw rows its own lane 0 loaded.
+            static_assert(BN == 128 && R::kLoadWarps == 8,
+                          "the predicated-load producer is laid out for 128 x 128 tiles, 8 warps");
+            constexpr int kRaw = T::kRawStages;
+            constexpr uint32_t kRawRowA = T::kRawRowA, kRawRowB = T::kRawRowB;
+            constexpr uint32_t kResA = 16 * kRawRowA;     // one residue's A rows: 2304 B
+            constexpr uint32_t kResB = 8 * kRawRowB;      // one residue's B k-rows: 2176 B
+            const int g8 = lane >> 3, c8 = lane & 7;
+            const int g16 = lane >> 4, c16 = lane & 15;
+            const bool has_a = p.M > warp, has_b = p.K > warp;   // residue has rows at all
+            const uint32_t tx = (has_a ? kResA : 0u) + (has_b ? kResB : 0u);
+            const Shift fa = make_shift((uint32_t)((reinterpret_cast<uintptr_t>(p.A) +
+                                                    2ull * (uint64_t)warp * (uint64_t)p.K) & 15u));
+            const Shift fb = make_shift((uint32_t)((reinterpret_cast<uintptr_t>(p.B) +
+                                                    2ull * (uint64_t)warp * (uint64_t)p.N) & 15u));
+            const CUtensorMap *map_a = &rm.a[warp];
+            const CUtensorMap *map_b = &rm.b[warp];
+            if (lane == 0) {
+                if (has_a)
+                    tma_prefetch_map(map_a);
+                if (has_b)
+                    tma_prefetch_map(map_b);
             }
+            auto raw_bar = [&](uint32_t j) { return drain_bar + 8u * (1u + (uint32_t)warp * kRaw + j); };
+            const int64_t items = num_items(p, blockIdx.x, gridDim.x);
+            struct Cursor {
+                int64_t it;
+                int m0, n0, kb, kb0, kb1;
+            };
+            auto open = [&](Cursor &cu, int64_t i) {
+                int64_t t, mb, nb;
+                int kind;
+                item_at(p, blockIdx.x, gridDim.x, i, t, cu.kb0, cu.kb1, kind);
+                tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
+                cu.it = i;
+                cu.kb = cu.kb0;
+                cu.m0 = (int)(mb * BM);
+                cu.n0 = (int)(nb * BN);
+            };
+            auto advance = [&](Cursor &cu) -> bool {
+                if (++cu.kb < cu.kb1)
+                    return true;
+                if (cu.it + 1 >= items)
+                    return false;
+                open(cu, cu.it + 1);
+                return true;
+            };
+            // stage `cu`'s rows of this residue into raw slot j
+            auto issue = [&](const Cursor &cu, uint32_t j) {
+                if (lane != 0)
+                    return;
+                const uint32_t rb = raw_bar(j);
+                const uint32_t raw = base + T::kOffRaw + j * T::kRawStage;
+                if (tx == 0u) {
+                    mbar_arrive(rb);
+                    return;
+                }
+                mbar_arrive_expect_tx(rb, tx);
+                if (has_a)
+                    tma_load_2d(map_a, raw + (uint32_t)warp * kResA, rb, cu.kb * BK, cu.m0 / 8);
+                if (has_b)
+                    tma_load_2d(map_b, raw + T::kRawB + (uint32_t)warp * kResB, rb, cu.n0,
+                                cu.kb * (BK / 8));
+            };
+            // raw slot j -> operand stage `stage`: all sixteen block reads
+            // first, then the shifts and stores.  (Reading one block and
+            // taking the next from the neighbour lane with shuffles measured
+            // slower: the shuffles share the shared-memory pipe.)
+            auto fix_stage = [&](uint32_t j, uint32_t stage) {
+                const uint32_t raw = base + T::kOffRaw + j * T::kRawStage;
+                const uint32_t adst = base + kOffA + stage * kATile;
+                const uint32_t bdst = base + kOffB + stage * kBTile;
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                uint4 v[8][2];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t sa = raw + (uint32_t)warp * kResA +
+                                        (uint32_t)(4 * t + g8) * kRawRowA + 16u * (uint32_t)c8;
+                    v[t][0] = ld_shared_v4(sa);
+                    v[t][1] = ld_shared_v4(sa + 16u);
+                    const uint32_t sb = raw + T::kRawB + (uint32_t)warp * kResB +
+                                        (uint32_t)(2 * t + g16) * kRawRowB + 16u * (uint32_t)c16;
+                    v[4 + t][0] = ld_shared_v4(sb);
+                    v[4 + t][1] = ld_shared_v4(sb + 16u);
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint4 o = has_a ? window16(v[t][0], v[t][1], fa) : z;
+                    st_shared_v4(adst + sw128_offset((uint32_t)(warp + 8 * (4 * t + g8)), (uint32_t)c8),
+                                 o.x, o.y, o.z, o.w);
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint4 o = has_b ? window16(v[4 + t][0], v[4 + t][1], fb) : z;
+                    st_shared_v4(bdst + (uint32_t)(c16 >> 3) * kBSlab +
+                                     sw128_offset((uint32_t)(warp + 8 * (2 * t + g16)),
+                                                  (uint32_t)(c16 & 7)),
+                                 o.x, o.y, o.z, o.w);
+                }
+            };
+            Cursor cp{}, fx{};
+            bool cp_more = items > 0, fx_more = items > 0;
+            if (cp_more) {
+                open(cp, 0);
+                fx = cp;
+            }
+            uint32_t issued = 0, fixed = 0;      // stages loaded / shifted by this warp
+            for (int i = 0; i < kRaw - 1 && cp_more; ++i) {
+                issue(cp, issued % kRaw);
+                ++issued;
+                cp_more = advance(cp);
+            }
+            uint32_t stage = 0, phase = 0;
+            while (fx_more) {
+                // the next load goes into the slot shifted last (read complete:
+                // ordered by that stage's proxy fence and __syncwarp)
+                if (cp_more) {
+                    issue(cp, issued % kRaw);
+                    ++issued;
+                    cp_more = advance(cp);
+                }
+                const uint32_t j = fixed % kRaw;
+                bool ok = true;
+                // (both usually complete already: poll without the suspend
+                // hint, which measured faster here)
+                if (lane == 0)
+                    ok = wait_bounded_eager(raw_bar(j), (fixed / kRaw) & 1u, p.wait_limit_ns,
+                                            abort_flag, kSiteProducerEmpty) &&
+                         wait_bounded_eager(empty_bar(stage), phase ^ 1u, p.wait_limit_ns,
+                                            abort_flag, kSiteProducerEmpty);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
+                    break;
+                fix_stage(j, stage);
+                // every lane's stores made visible to the tensor core (and its
+                // raw reads ordered before the next TMA write of the slot),
+                // then one arrival per warp
+                fence_proxy_async_smem();
+                __syncwarp();
+                const bool drop = p.drop_arrive && blockIdx.x == 0 && fx.it == 0 && fx.kb == fx.kb0;
+                if (lane == 0 && !drop)
+                    mbar_arrive(full_bar(stage));
+                ++fixed;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                fx_more = advance(fx);
+            }
+            // loads still in flight after an abort must land before the CTA exits
+            if (lane == 0)
+                for (uint32_t q = fixed; q < issued; ++q)
+                    wait_drain(raw_bar(q % kRaw), (q / kRaw) & 1u, p.wait_limit_ns, abort_flag);
         }
     } else if (warp == R::kMmaWarp) {
         // ============================================================ MMA issuer
@@ -649,7 +850,8 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         int last_kb0 = 0, last_kb1 = 0, last_kind = kItemFull;
         if (items > 0)
             item_at(p, blockIdx.x, gridDim.x, items - 1, last_t, last_kb0, last_kb1, last_kind);
-        const bool preload = last_kind == kItemPieceIn && items >= 2;
+        // (stream-K runs on the TMA path only)
+        const bool preload = kTma && last_kind == kItemPieceIn && items >= 2;
         const uint32_t partner_buf = tmem_base + lane_base + (uint32_t)((items - 2) & 1) * BN;
         auto preload_piece = [&]() -> bool {
             uint32_t *flag = p.sk_flags + (blockIdx.x + 1) * 4 + q;
@@ -669,14 +871,18 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             int kb0, kb1, kind;
             item_at(p, blockIdx.x, gridDim.x, i, t, kb0, kb1, kind);
             const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
-            const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
-                                         kSiteEpiAccFull);
+            // (the predicated-load kernel's producers share the schedulers
+            // with these warps: poll slowly there)
+            const bool ok = kTma ? wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
+                                                kSiteEpiAccFull)
+                                 : wait_bounded_sleep(accf_bar(buf), use, p.wait_limit_ns,
+                                                      abort_flag, kSiteEpiAccFull, 256);
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after_sync();
             const uint32_t acc = tmem_base + lane_base + buf * BN;
             const bool preload_next = preload && i == items - 2;
-            if (kind == kItemPieceOut) {
+            if (kTma && kind == kItemPieceOut) {
                 // k tail of a tile cut with the previous CTA: publish the raw
                 // fp32 piece in this CTA's slot.
                 float *slot = p.sk_part + (size_t)blockIdx.x * BN * BM;
@@ -710,13 +916,13 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 uint32_t r[32], h[32];
                 const uint32_t taddr = acc + 64 * c;
                 tmem_ld_x32_sync(taddr, r);
-                if (kind == kItemPieceIn)
+                if (kTma && kind == kItemPieceIn)
                     add_tmem(r, partner_buf + 64 * c);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
                 tmem_ld_x32_sync(taddr + 32, r);
-                if (kind == kItemPieceIn)
+                if (kTma && kind == kItemPieceIn)
                     add_tmem(r, partner_buf + 64 * c + 32);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
@@ -757,10 +963,14 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                                                          ((((uint32_t)lane >> 2) ^ (rr & 7u)) << 4) +
                                                          ((uint32_t)lane & 3u) * 4u);
                         uint16_t *dst = p.C + row * p.N + col;
-                        if (col < p.N)
-                            dst[0] = (uint16_t)(w & 0xffffu);
-                        if (col + 1 < p.N)
-                            dst[1] = (uint16_t)(w >> 16);
+                        if (col + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+                            *reinterpret_cast<uint32_t *>(dst) = w;
+                        } else {
+                            if (col < p.N)
+                                dst[0] = (uint16_t)(w & 0xffffu);
+                            if (col + 1 < p.N)
+                                dst[1] = (uint16_t)(w >> 16);
+                        }
                     }
                     __syncwarp();
                 }
