@@ -73,25 +73,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// ---------------------------------------------------------------- cp.async
-
-// 16-byte asynchronous global -> shared copy (bypassing L1); the bytes past
-// `src_bytes` (0 or 16) are written as zeros without being read.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// ---------------------------------------------------------------- shared memory
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
