@@ -180,10 +180,15 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
  *
  * Scratch: GEMMRELU_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory in a
  * static device array.  Every GPU that loads the library holds it until the
- * process exits.  A problem needs
- * gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes of it; larger
- * problems are rejected with GEMMRELU_ERR_SCRATCH_LIMIT and nothing is
- * launched.  (16 x 8192 x 8192 at split_k 8 needs 4 MiB.)
+ * process exits.  Only the two-stage form of gemm_relu_f16_splitk uses it:
+ * a call that runs that form needs
+ * gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k) bytes of it, and
+ * if that is more than the array holds the call returns
+ * GEMMRELU_ERR_SCRATCH_LIMIT and launches nothing.  Calls that run the
+ * CTA-pair form or fall back to the unsplit kernel (split_k clamped to 1, or
+ * operands that cannot use TMA) need no scratch and run whatever the
+ * workspace query says.  (16 x 8192 x 8192 at split_k 8 takes the CTA-pair
+ * form; forced into the two-stage form it needs 4 MiB.)
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current.  Make that first call
@@ -197,9 +202,10 @@ int gemm_relu_f16_splitk(const void *A, const void *B, void *C,
  * (for example on two streams without ordering between them) race on the
  * array and give undefined results: order them on one stream or with events.
  *
- * Everything else -- arguments, layouts, alignment, the fallback to the
- * unsplit kernel when split_k == 1 or the operands cannot use TMA, status
- * reporting -- is as for gemm_relu_f16_splitk.
+ * Everything else -- arguments, layouts, alignment, the choice of form, the
+ * fallback to the unsplit kernel, status reporting -- is as for
+ * gemm_relu_f16_splitk, and so are the result's bits.  The test hooks below
+ * must not change while a call is being made.
  */
 #define GEMMRELU_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 int gemm_relu_f16_splitk_noalloc(const void *A, const void *B, void *C,

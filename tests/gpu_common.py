@@ -65,3 +65,26 @@ def assert_parity(g, o, absab, K, what=""):
     assert r["contract_ok"], (what, r)
     assert r["strict_ok"], (what, r)
     return r
+
+
+def oracle_threaded(orc, A, B, threads=None):
+    """The oracle's full output, its rows split over host threads (the oracle
+    library releases the GIL; every row is computed on its own, in the same
+    order as a single call would)."""
+    import os
+    import threading
+    M = A.shape[0]
+    threads = threads or os.cpu_count() or 1
+    out = np.empty((M, B.shape[1]), dtype=np.float16)
+    step = (M + threads - 1) // threads
+
+    def work(r0):
+        n = min(step, M - r0)
+        if n > 0:
+            out[r0:r0 + n] = orc.gemm_relu_f16_rows(A, B, r0, n)
+    pool = [threading.Thread(target=work, args=(r0,)) for r0 in range(0, M, step)]
+    for t in pool:
+        t.start()
+    for t in pool:
+        t.join()
+    return out

@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path against the CPU oracle, element by element.
 
-Sizes the oracle finishes in seconds are compared in full; the 4096^3 case
-is compared on sampled rows and elements (plus full-size properties).  The
+Every workload is compared in full, the 4096^3 one with the oracle's rows
+spread over the host's threads (computed once per module); the stream-K
+shapes other than 4096^3 are compared on sampled rows and elements.  The
 tolerance is atol = rtol = 1e-2 per element, and every case must also meet
 the scale-aware bound of gpu_common.compare.
 """
@@ -11,7 +12,7 @@ import pytest
 import tiled_tensor_core_03_gb300 as gr
 from tiled_tensor_core_03_gb300 import inputs
 
-from gpu_common import abs_dot, assert_parity, dev, host, run_fused, run_split
+from gpu_common import abs_dot, assert_parity, dev, host, oracle_threaded, run_fused, run_split
 
 pytestmark = pytest.mark.gpu
 
@@ -50,31 +51,29 @@ def test_ragged_takes_lsu_path_and_aligned_takes_tma():
     assert gr.gemm_relu_f16_path(a.data_ptr(), a.data_ptr(), a.data_ptr(), 1024, 1024, 1024) == gr.PATH_TMA
 
 
-def test_square4096_sampled(orc):
-    import torch
+@pytest.fixture(scope="module")
+def square4096(orc):
+    """The 4096^3 workload, its full oracle output (rows over the host's
+    threads) and sum_k |a||b| for the scale-aware bound."""
     w = inputs.WORKLOADS["square4096"]
     A, B = inputs.make_workload(w)
+    return w, A, B, oracle_threaded(orc, A, B), abs_dot(A, B)
+
+
+def test_square4096_full(square4096):
+    """Every element of the 4096^3 output against the oracle."""
+    import torch
+    w, A, B, want, absab = square4096
     a, b = dev(A), dev(B)
     c = gr.gemm_relu(a, b)
     got = host(c)
-    # full-size properties
-    assert np.isfinite(got.astype(np.float32)).all()
-    assert (got.astype(np.float32) >= 0).all()
-    # cross-check against cuBLAS fp32 over the whole output (test-only)
-    ref32 = torch.relu(a.float() @ b.float())
-    torch.testing.assert_close(c.float(), ref32, rtol=1e-2, atol=1e-2)
-    # oracle on rows spanning every 128-row block (first and last row of each)
-    rows = sorted({r for mb in range(w.M // 128) for r in (mb * 128, mb * 128 + 127)} | {1, 4095})
-    for r0 in range(0, len(rows), 16):
-        rr = rows[r0:r0 + 16]
-        want = np.concatenate([orc.gemm_relu_f16_rows(A, B, r, 1) for r in rr])
-        assert_parity(got[rr], want, abs_dot(A[rr], B), w.K, f"rows {rr[0]}..")
-    # and random elements everywhere
-    rng = np.random.default_rng(99)
-    I = rng.integers(0, w.M, 4096)
-    J = rng.integers(0, w.N, 4096)
-    want = orc.gemm_relu_f16_at(A, B, I, J)
-    assert_parity(got[I, J], want, abs_dot(A, B, I, J), w.K, "samples")
+    assert_parity(got, want, absab, w.K, "square4096")
+    # the stream-K call (the benchmark's path) on the same operands
+    ws = gr.streamk_workspace(w.M, w.N, w.K)
+    ws.random_(0, 256)
+    got_sk = host(gr.gemm_relu_streamk(a, b, workspace=ws))
+    assert gr.status() == gr.OK
+    assert_parity(got_sk, want, absab, w.K, "square4096 stream-K")
 
 
 def test_skinny_splitk_full(orc):
@@ -373,11 +372,16 @@ def test_each_kernel_sweep_and_workloads(orc, forced_kernel):
 
 
 @pytest.mark.parametrize("forced_kernel", sorted(KERNELS), indirect=True)
-def test_each_kernel_square4096_sampled(orc, forced_kernel):
-    w = inputs.WORKLOADS["square4096"]
-    A, B = inputs.make_workload(w)
-    got = run_fused(A, B)
-    _sampled_parity(orc, A, B, got, (forced_kernel, "square4096"))
+def test_each_kernel_square4096_full(square4096, forced_kernel):
+    """Every element of the 4096^3 output of each kernel, plain and with the
+    stream-K schedule, against the oracle."""
+    w, A, B, want, absab = square4096
+    a, b = dev(A), dev(B)
+    assert_parity(host(gr.gemm_relu(a, b)), want, absab, w.K, (forced_kernel, "square4096"))
+    if gr.gemm_relu_f16_streamk_workspace_bytes(w.M, w.N, w.K) > 0:
+        got = host(gr.gemm_relu_streamk(a, b, workspace=gr.streamk_workspace(w.M, w.N, w.K)))
+        assert_parity(got, want, absab, w.K, (forced_kernel, "square4096 stream-K"))
+    assert gr.status() == gr.OK
 
 
 @pytest.mark.parametrize("forced_kernel", ["cta_pair"], indirect=True)

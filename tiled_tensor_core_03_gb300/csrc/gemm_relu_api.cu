@@ -730,6 +730,52 @@ int noalloc_scratch(void **out) {
     return GEMMRELU_OK;
 }
 
+// gemm_relu_f16_splitk and gemm_relu_f16_splitk_noalloc: one routing
+// decision and one layout per call.  With `noalloc`, the partials of the
+// two-stage form go to g_noalloc_scratch instead of a caller workspace; the
+// other forms need no scratch, so only the two-stage form is held to the
+// array's size.
+int splitk_run(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int split_k,
+               void *workspace, size_t workspace_bytes, bool noalloc, cudaStream_t s) {
+    int rc = check_args(A, B, C, M, N, K);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    if (split_k < 1)
+        return GEMMRELU_ERR_WORKSPACE;
+    if (M == 0 || N == 0)
+        return GEMMRELU_OK;
+    DeviceState *ds = nullptr;
+    rc = current_device_state(&ds);
+    if (rc != GEMMRELU_OK)
+        return rc;
+    if (K == 0)
+        return zero_fill(C, M, N, s);
+    const SplitLayout L = split_layout(M, N, K, split_k);
+    if (L.splits <= 1 || !tma_ok(A, K) || !tma_ok(B, N))
+        return launch_fused(A, B, C, M, N, K, s, ds);
+    const size_t need = (size_t)L.part_bytes;
+    if (noalloc && need > 0) {
+        if (need > GEMMRELU_NOALLOC_SCRATCH_BYTES)
+            return GEMMRELU_ERR_SCRATCH_LIMIT;
+        rc = noalloc_scratch(&workspace);
+        if (rc != GEMMRELU_OK)
+            return rc;
+        workspace_bytes = GEMMRELU_NOALLOC_SCRATCH_BYTES;
+    }
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return GEMMRELU_ERR_WORKSPACE;
+    switch (L.bms) {
+    case 16:
+        return launch_split_bms<16>(A, B, C, M, N, K, L, workspace, s, ds, 0);
+    case 32:
+        return launch_split_bms<32>(A, B, C, M, N, K, L, workspace, s, ds, 1);
+    case 64:
+        return launch_split_bms<64>(A, B, C, M, N, K, L, workspace, s, ds, 2);
+    default:
+        return launch_split_bms<128>(A, B, C, M, N, K, L, workspace, s, ds, 3);
+    }
+}
+
 }  // namespace
 
 // ==================================================================== C ABI
@@ -803,58 +849,14 @@ size_t gemm_relu_f16_splitk_workspace_bytes(int64_t M, int64_t N, int64_t K, int
 
 int gemm_relu_f16_splitk(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                          int split_k, void *workspace, size_t workspace_bytes, void *stream) {
-    int rc = check_args(A, B, C, M, N, K);
-    if (rc != GEMMRELU_OK)
-        return rc;
-    if (split_k < 1)
-        return GEMMRELU_ERR_WORKSPACE;
-    if (M == 0 || N == 0)
-        return GEMMRELU_OK;
-    DeviceState *ds = nullptr;
-    rc = current_device_state(&ds);
-    if (rc != GEMMRELU_OK)
-        return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0)
-        return zero_fill(C, M, N, s);
-    const SplitLayout L = split_layout(M, N, K, split_k);
-    if (L.splits <= 1 || !tma_ok(A, K) || !tma_ok(B, N))
-        return launch_fused(A, B, C, M, N, K, s, ds);
-    const size_t need = (size_t)L.part_bytes;
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
-        return GEMMRELU_ERR_WORKSPACE;
-    switch (L.bms) {
-    case 16:
-        return launch_split_bms<16>(A, B, C, M, N, K, L, workspace, s, ds, 0);
-    case 32:
-        return launch_split_bms<32>(A, B, C, M, N, K, L, workspace, s, ds, 1);
-    case 64:
-        return launch_split_bms<64>(A, B, C, M, N, K, L, workspace, s, ds, 2);
-    default:
-        return launch_split_bms<128>(A, B, C, M, N, K, L, workspace, s, ds, 3);
-    }
+    return splitk_run(A, B, C, M, N, K, split_k, workspace, workspace_bytes, false,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int gemm_relu_f16_splitk_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
                                  int64_t K, int split_k, void *stream) {
-    int rc = check_args(A, B, C, M, N, K);
-    if (rc != GEMMRELU_OK)
-        return rc;
-    if (split_k < 1)
-        return GEMMRELU_ERR_WORKSPACE;
-    if (M == 0 || N == 0)
-        return GEMMRELU_OK;
-    const size_t need = gemm_relu_f16_splitk_workspace_bytes(M, N, K, split_k);
-    if (need > GEMMRELU_NOALLOC_SCRATCH_BYTES)
-        return GEMMRELU_ERR_SCRATCH_LIMIT;
-    void *scratch = nullptr;
-    if (need > 0) {
-        rc = noalloc_scratch(&scratch);
-        if (rc != GEMMRELU_OK)
-            return rc;
-    }
-    return gemm_relu_f16_splitk(A, B, C, M, N, K, split_k, scratch,
-                                need > 0 ? GEMMRELU_NOALLOC_SCRATCH_BYTES : 0, stream);
+    return splitk_run(A, B, C, M, N, K, split_k, nullptr, 0, true,
+                      static_cast<cudaStream_t>(stream));
 }
 
 int flash_attention_f16(const void *Q, const void *K, const void *V, void *O, int64_t batch,
@@ -864,8 +866,11 @@ int flash_attention_f16(const void *Q, const void *K, const void *V, void *O, in
         return GEMMRELU_ERR_INVALID_ARG;
     if (batch == 0 || seq == 0 || heads == 0)
         return GEMMRELU_OK;
+    // batch * heads * head_dim <= 65535^2 * 128 < 2^39 fits; the element
+    // count is bounded by 2^40 without forming the product with seq
+    const int64_t bhd = batch * heads * head_dim;
     if (!Q || !K || !V || !O || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) ||
-        !aligned(O, 16) || batch * seq * heads * head_dim > ((int64_t)1 << 40))
+        !aligned(O, 16) || seq > ((int64_t)1 << 40) / bhd)
         return GEMMRELU_ERR_INVALID_ARG;
     DeviceState *ds = nullptr;
     int rc = current_device_state(&ds);
