@@ -47,6 +47,7 @@ L2_CLEAN_BYTES = 256 << 20       # then read, so no dirty flush lines remain in 
 INPUT_SETS = 3                   # operand copies each headline part rotates through
 ROTATE_BYTES = 256 << 20         # small workloads rotate through at least this many operand bytes
 PART_LOOP_S = 1.0                # per-part loops run at least this long (clock samples)
+HOLD_S = 2e-3                    # GPU-side hold before a timed region (the host queues ahead)
 SOAK_S = 1.2                     # clock soak of the step
 
 METRIC = "GEMM+ReLU TFLOP/s (fp16 in, fp32 acc)"
@@ -512,11 +513,19 @@ class Gpu:
         E = self.torch.cuda.Event
         return E(enable_timing=True), E(enable_timing=True)
 
+    def hold(self):
+        """Keep the launch stream busy for about HOLD_S (a spinning torch
+        kernel) so that the launches the host queues next are already waiting
+        when the start event is recorded behind it: the timed region then
+        measures the GPU, not the host's launch rate after an idle spell."""
+        self.torch.cuda._sleep(int(HOLD_S * 2.1e9))
+
     def time_stream(self, launch, nsets, n):
-        """n launches back to back on the launch stream (set i % nsets);
-        events at both ends.  Returns ms per launch."""
+        """n launches back to back on the launch stream (set i % nsets),
+        queued behind a hold; events at both ends.  Returns ms per launch."""
         e0, e1 = self.events()
         self.sync()
+        self.hold()
         e0.record(self.stream)
         for i in range(n):
             launch(i % nsets, self.stream)
@@ -564,6 +573,12 @@ class Gpu:
             self.sync()
             out.append(e0.elapsed_time(e1))
         return out
+
+    def cold_floor_ms(self, n=10):
+        """The cold-launch method around a one-element torch kernel: what a
+        single launch between two events costs on this GPU before any work."""
+        tiny = self.torch.zeros(1, device=self.device)
+        return statistics.median(self.time_cold(lambda r, s: tiny.add_(1), n))
 
     def time_loop(self, launch, nsets, seconds, est_ms):
         """Launches back to back for about `seconds` (at least 20), clocks
@@ -717,6 +732,7 @@ def measure_step(gpu, args, world, parts, name):
     e_start, e_end = gpu.events()
     barrier(world)
     gpu.sync()
+    gpu.hold()
     sampler.mark("t_start")
     wall0 = time.perf_counter()
     e_start.record(stream)
@@ -754,11 +770,13 @@ def measure_step(gpu, args, world, parts, name):
     # ---- cold launches: L2 flushed before each, events around each alone
     cold_ms = {label: gpu.time_cold(launch[label], max(3, min(args.steps, 10)))
                for label, _, _ in parts}
+    cold_floor = gpu.cold_floor_ms()
     check_status(gr, stream, "after cold launches")
     # ---- clock soak: the step back to back for SOAK_S, clocks sampled
     t0 = time.time()
     n_soak = max(20, int(SOAK_S / (step_ms * 1e-3)))
     e0, e1 = gpu.events()
+    gpu.hold()
     e0.record(stream)
     for i in range(n_soak):
         for label, _, _ in parts:
@@ -840,14 +858,16 @@ def measure_step(gpu, args, world, parts, name):
                    f"every launch by a {L2_FLUSH_BYTES >> 20} MiB write and a "
                    f"{L2_CLEAN_BYTES >> 20} MiB read of other buffers"),
             "timing": "steps back to back on one stream, each kernel launched with "
-                      "programmatic stream serialisation; value and ms_per_step from CUDA "
+                      "programmatic stream serialisation, queued behind a ~2 ms GPU-side "
+                      "hold recorded before the start event (the host's launch latency after "
+                      "an idle spell stays out of the region); value and ms_per_step from CUDA "
                       "events at the two ends of the timed region only; parts (and roofline): "
                       "each part alone, K launches back to back on the rotating input sets, "
                       f"events at both ends; parts.sustained: the same for at least "
                       f"{PART_LOOP_S:.0f} s with the clocks sampled (power cap), against the "
                       f"sustained peak; cold_launch: L2 flushed, "
                       "events around each launch alone (includes the launch latency an idle "
-                      "GPU pays)",
+                      "GPU pays; floor_ms: the same method around a one-element torch kernel)",
         },
         "roofline": roofs[dominant],
         "parts": {label: {"ms": part_ms[label],
@@ -860,7 +880,8 @@ def measure_step(gpu, args, world, parts, name):
                                 "tflops": w.flops / (statistics.mean(cold_ms[label]) * 1e-3) / 1e12,
                                 "gbs": w.bytes / (statistics.mean(cold_ms[label]) * 1e-3) / 1e9,
                                 "frac": cold_roofs[label]["frac"],
-                                "bound": cold_roofs[label]["bound"]}
+                                "bound": cold_roofs[label]["bound"],
+                                "floor_ms": cold_floor}
                         for label, w, _ in parts},
         "warm_launch": {label: {"ms": warm_ms[label],
                                 "tflops": w.flops / (warm_ms[label] * 1e-3) / 1e12,

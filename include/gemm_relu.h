@@ -275,6 +275,16 @@ int gemm_relu_debug_force_kernel(int which);
  */
 int gemm_relu_debug_force_split(int which);
 
+/*
+ * gemm_relu_debug_set_panel -- test hook.  Sets the height of the tile
+ * rasteriser's panels (see gemm_relu_tile_coord) in output rows: a multiple
+ * of 128, or 0 for the library's own choice (default).  Every panel height
+ * gives the same results; it changes only the order in which tiles are
+ * computed, and so L2 reuse.  Affects the calling process only.  Returns
+ * GEMMRELU_OK, or GEMMRELU_ERR_INVALID_ARG for another value.
+ */
+int gemm_relu_debug_set_panel(int rows);
+
 #ifdef __cplusplus
 }
 #endif

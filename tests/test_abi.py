@@ -47,6 +47,13 @@ def test_strerror(lib):
     assert gr.strerror(999) == "unknown status"
 
 
+def test_panel_hook_arguments(lib):
+    assert gr.gemm_relu_debug_set_panel(-128) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_debug_set_panel(200) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_debug_set_panel(384) == gr.OK
+    assert gr.gemm_relu_debug_set_panel(0) == gr.OK
+
+
 def test_invalid_arguments_rejected_on_host(lib):
     c = 0x1000
     assert gr.gemm_relu_f16(c, c, c, -1, 4, 4) == gr.ERR_INVALID_ARG

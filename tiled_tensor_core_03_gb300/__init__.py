@@ -73,6 +73,8 @@ def lib():
         L.gemm_relu_debug_force_split.restype = i32
         L.flash_attention_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i32, vp]
         L.flash_attention_f16.restype = i32
+        L.gemm_relu_debug_set_panel.argtypes = [i32]
+        L.gemm_relu_debug_set_panel.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
         L.gemm_relu_debug_set.restype = i32
         _lib = L
@@ -150,6 +152,10 @@ SPLIT_AUTO, SPLIT_TWO_STAGE = 0, 1
 
 def gemm_relu_debug_force_split(which):
     return lib().gemm_relu_debug_force_split(int(which))
+
+
+def gemm_relu_debug_set_panel(rows):
+    return lib().gemm_relu_debug_set_panel(int(rows))
 
 
 def gemm_relu_debug_set(drop_arrive=0, wait_limit_ns=0):

@@ -62,6 +62,7 @@ constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
 constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 227u * 1024u, "pair kernel: shared memory over the per-CTA limit");
 
 // A K-major, B N-major; M = 256 across the pair, N = 256.
 constexpr uint32_t kIdesc = make_idesc_f16_f32(BMP, BNP, 0, 1);
