@@ -100,19 +100,20 @@ size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * over all CTAs along K.  Here all full waves but the last run data-parallel
  * (one 128 x 256 tile per CTA at a time); the k blocks of the remaining
  * tiles are divided into one equal contiguous range per CTA.  A tile cut
- * between two CTAs is finished by the CTA holding its first k blocks, which
- * adds the other CTA's fp32 piece (passed through `workspace`) before the
- * ReLU and the fp16 store.  Each tile is cut at most once, so the result is
- * the same from run to run.
+ * between two CTAs is summed as (first k blocks) + (last k blocks) in fp32
+ * before the ReLU and the fp16 store, by whichever of the two CTAs finishes
+ * its part second: each publishes its fp32 piece through `workspace` unless
+ * the other's is already there, and neither ever waits for the other, so
+ * the kernel needs no guarantee that its CTAs run at the same time.  Each
+ * tile is cut at most once and fp32 addition is commutative, so the result
+ * is the same from run to run.
  *
  * workspace: device buffer of at least
  *            gemm_relu_f16_streamk_workspace_bytes(M, N, K) bytes, 16-byte
  *            aligned; its contents need no initialisation.  Calls that may
  *            run concurrently on the GPU must use distinct workspaces.
- * The launch is cooperative (all CTAs resident at once); it fails with
- * GEMMRELU_ERR_LAUNCH if the GPU cannot host the whole grid.  When the
- * tiles already fill whole waves, or the operands cannot use TMA, the call
- * runs gemm_relu_f16's kernel and leaves the workspace untouched.
+ * When the tiles already fill whole waves, or the operands cannot use TMA,
+ * the call runs gemm_relu_f16's kernel and leaves the workspace untouched.
  */
 int gemm_relu_f16_streamk(const void *A, const void *B, void *C,
                           int64_t M, int64_t N, int64_t K,
@@ -284,6 +285,19 @@ int gemm_relu_debug_force_split(int which);
  * GEMMRELU_OK, or GEMMRELU_ERR_INVALID_ARG for another value.
  */
 int gemm_relu_debug_set_panel(int rows);
+
+/*
+ * gemm_relu_debug_streamk -- test hook for the stream-K fix-up of a tile cut
+ * between two workers.  0 (default): the side that holds the tile's first k
+ * blocks adds the other side's published piece when it is already there.
+ * 1: that side always publishes its own piece first, so the second side to
+ * arrive finishes the tile from global memory.  2: as 1, and the side that
+ * holds the last k blocks also waits about 0.2 ms before publishing, so the
+ * other order of arrival is exercised.  All modes give the same bits.
+ * Affects the calling process only.  Returns GEMMRELU_OK, or
+ * GEMMRELU_ERR_INVALID_ARG for another value.
+ */
+int gemm_relu_debug_streamk(int mode);
 
 #ifdef __cplusplus
 }

@@ -47,6 +47,13 @@ def test_strerror(lib):
     assert gr.strerror(999) == "unknown status"
 
 
+def test_streamk_hook_arguments(lib):
+    assert gr.gemm_relu_debug_streamk(3) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_debug_streamk(-1) == gr.ERR_INVALID_ARG
+    for mode in (gr.SK_TAIL_LATE, gr.SK_HEAD_PUBLISHES, gr.SK_NORMAL):
+        assert gr.gemm_relu_debug_streamk(mode) == gr.OK
+
+
 def test_panel_hook_arguments(lib):
     assert gr.gemm_relu_debug_set_panel(-128) == gr.ERR_INVALID_ARG
     assert gr.gemm_relu_debug_set_panel(200) == gr.ERR_INVALID_ARG

@@ -339,6 +339,35 @@ def test_streamk_parity(orc, sk_kernel, M, N, K):
     torch.testing.assert_close(c.float(), ref.float(), rtol=1e-2, atol=1e-3)
 
 
+@pytest.mark.parametrize("M,N,K", STREAMK_SHAPES[1:])
+def test_streamk_fixup_orders_give_identical_bits(orc, sk_kernel, M, N, K):
+    """The fix-up of a cut tile gives the same bits whichever side finishes
+    it: the first k blocks' side adding a pre-loaded piece (normal), adding a
+    published piece from global memory after publishing its own first (the
+    other side then being second), or the last k blocks' side finishing
+    because it publishes late.  Every mode is also checked against the oracle
+    on sampled rows and elements."""
+    import torch
+    A, B = inputs.make(M, N, K, "normal", True, seed=M + 2 * N + K)
+    a, b = dev(A), dev(B)
+    ws = gr.streamk_workspace(M, N, K)
+    outs = {}
+    try:
+        for mode in (gr.SK_NORMAL, gr.SK_HEAD_PUBLISHES, gr.SK_TAIL_LATE, gr.SK_NORMAL):
+            assert gr.gemm_relu_debug_streamk(mode) == gr.OK
+            ws.random_(0, 256)
+            c = gr.gemm_relu_streamk(a, b, workspace=ws)
+            assert gr.status() == gr.OK
+            if mode in outs:
+                assert torch.equal(c.view(torch.int16), outs[mode].view(torch.int16)), mode
+            outs[mode] = c
+    finally:
+        gr.gemm_relu_debug_streamk(gr.SK_NORMAL)
+    for mode, c in outs.items():
+        assert torch.equal(c.view(torch.int16), outs[gr.SK_NORMAL].view(torch.int16)), mode
+        _sampled_parity(orc, A, B, host(c), (M, N, K, "fix-up mode", mode))
+
+
 def test_streamk_falls_back_without_a_cut():
     import torch
     # 1024 x 2048 x 512: 32 tiles, fewer than the SMs -> plain kernel, no workspace

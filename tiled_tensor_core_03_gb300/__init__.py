@@ -73,6 +73,8 @@ def lib():
         L.gemm_relu_debug_force_split.restype = i32
         L.flash_attention_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i32, vp]
         L.flash_attention_f16.restype = i32
+        L.gemm_relu_debug_streamk.argtypes = [i32]
+        L.gemm_relu_debug_streamk.restype = i32
         L.gemm_relu_debug_set_panel.argtypes = [i32]
         L.gemm_relu_debug_set_panel.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
@@ -152,6 +154,13 @@ SPLIT_AUTO, SPLIT_TWO_STAGE = 0, 1
 
 def gemm_relu_debug_force_split(which):
     return lib().gemm_relu_debug_force_split(int(which))
+
+
+SK_NORMAL, SK_HEAD_PUBLISHES, SK_TAIL_LATE = 0, 1, 2
+
+
+def gemm_relu_debug_streamk(mode):
+    return lib().gemm_relu_debug_streamk(int(mode))
 
 
 def gemm_relu_debug_set_panel(rows):

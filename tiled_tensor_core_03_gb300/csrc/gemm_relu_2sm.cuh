@@ -77,12 +77,16 @@ struct Params {
     uint64_t wait_limit_ns;
     // Stream-K over pairs, as in the single-CTA kernel: tiles [0, dp_tiles)
     // data-parallel, the k blocks of the rest cut into one range per pair.
-    // CTA b of a pair cut with the next pair passes its 128 rows of the
-    // tile's k tail through sk_part[b] / sk_flags[b][warp] to CTA b - 2.
+    // CTA b and CTA b + 2 (the same half of the next pair) meet on the rows
+    // of a cut tile through the wait-free exchange of the single-CTA kernel
+    // (fused::sk_exchange): k tail in sk_part[b + 2], k head in sk_head[b],
+    // state in sk_flags[b + 2][warp].
     int64_t dp_tiles;
-    float *sk_part;        // [2 * pairs] slots of 128 x BNP fp32, [BNP/4][128][4]
+    float *sk_part;        // [2 * pairs] k-tail slots of 128 x BNP fp32, [BNP/4][128][4]
+    float *sk_head;        // [2 * pairs] k-head slots, same layout
     uint32_t *sk_flags;    // [2 * pairs][4]
     uint32_t epoch;
+    int sk_mode;           // test hook, as in the single-CTA kernel
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -238,66 +242,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // accumulator buffer on the leader's acc_empty (remote for rank 1).
         const int ew = warp - 2;                // staging buffer owner 0..3
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
+        const int row_in_tile = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * 2u * kEpiBuf;
         uint32_t nstores = 0;
         const int64_t items = sk_num_items(sk, pair_id, num_pairs);
         const uint32_t acce_leader0 = mapa_shared(acce_bar(0), 0);
-        // Stream-K k head: pre-load the next pair's published k tail (this
-        // CTA's rows) into the spare TMEM buffer once the item before it has
-        // been read; the k head's epilogue adds the two buffers.  This CTA has
-        // published its own k tail (its pair's first stream-K item) by then.
+        // Stream-K: as in the single-CTA kernel, the next pair's published k
+        // tail (this CTA's rows) is pre-loaded into the spare TMEM buffer when
+        // it is already there once the item before the k head has been read;
+        // otherwise the two sides meet through the wait-free exchange.
         int64_t last_t = 0;
         int last_kb0 = 0, last_kb1 = 0, last_kind = kItemFull;
         if (items > 0)
             sk_item_at(sk, pair_id, num_pairs, items - 1, last_t, last_kb0, last_kb1, last_kind);
-        const bool preload = last_kind == kItemPieceIn && items >= 2;
+        const bool head_last = last_kind == kItemPieceIn;
         const uint32_t partner_buf = tmem_base + lane_base + (uint32_t)((items - 2) & 1) * BNP;
-        auto preload_piece = [&]() -> bool {
-            uint32_t *flag = p.sk_flags + (blockIdx.x + 2) * 4 + q;
-            const bool got = fused::wait_flag(flag, p.epoch, p.wait_limit_ns, abort_flag);
-            if (!__all_sync(0xffffffffu, got))
-                return false;
-            fused::piece_to_tmem<BNP>(p.sk_part + (size_t)(blockIdx.x + 2) * BNP * 128,
-                                      32 * q + lane, partner_buf);
+        constexpr size_t kSlot = (size_t)BNP * 128;
+        uint32_t *const head_cut = p.sk_flags + (blockIdx.x + 2) * 4 + q;
+        uint32_t *const tail_cut = p.sk_flags + blockIdx.x * 4 + q;
+        const float *const next_tail = p.sk_part + (size_t)(blockIdx.x + 2) * kSlot;
+        const float *const prev_head =
+            blockIdx.x >= 2 ? p.sk_head + (size_t)(blockIdx.x - 2) * kSlot : nullptr;
+        bool preloaded = false;
+        auto try_preload = [&]() {
+            if (p.sk_mode != 0 || fused::sk_peek(head_cut, lane) != fused::sk_tail_tag(p.epoch))
+                return;
+            fused::piece_to_tmem<BNP>(next_tail, row_in_tile, partner_buf);
             __syncwarp();
             if (lane == 0)
-                *flag = 0u;  // consumed: no later call can mistake it for its own
-            return true;
+                *head_cut = 0u;  // consumed
+            preloaded = true;
         };
-        for (int64_t i = 0; i < items; ++i) {
-            int64_t t;
-            int kb0, kb1, kind;
-            sk_item_at(sk, pair_id, num_pairs, i, t, kb0, kb1, kind);
-            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
-            const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
-                                         kSiteEpiAccFull);
-            if (!__all_sync(0xffffffffu, ok))
-                break;
-            tc_fence_after_sync();
-            const uint32_t acc = tmem_base + lane_base + buf * BNP;
-            if (kind == kItemPieceOut) {
-                // k tail of a tile cut with the previous pair: publish this
-                // CTA's 128 rows and raise this warp's flag
-                float *slot = p.sk_part + (size_t)blockIdx.x * BNP * 128;
+        auto publish = [&](float *slot, uint32_t acc) {
 #pragma unroll 1
-                for (int c = 0; c < BNP / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_x32_sync(acc + 32 * c, r);
-                    fused::piece_store32(slot, 32 * q + lane, 32 * c, r);
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    fused::st_release_gpu(p.sk_flags + blockIdx.x * 4 + q, p.epoch);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_cluster(acce_leader0 + 8u * buf);
-                if (preload && i == items - 2 && !preload_piece())
-                    break;
-                continue;
+            for (int c = 0; c < BNP / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_x32_sync(acc + 32 * c, r);
+                fused::piece_store32(slot, row_in_tile, 32 * c, r);
             }
+        };
+        // Stores this CTA's 128 rows of tile t from `acc` (+ the TMEM partner
+        // buffer when add == 1, + a published piece when add == 2).
+        auto store_tile = [&](int64_t t, uint32_t acc, int add, const float *piece) {
             int64_t mb, nb;
             tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
             const int64_t row0 = mb * BMP + 128 * (int64_t)rank + 32 * q;
@@ -310,14 +297,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 uint32_t r[32], h[32];
                 const uint32_t taddr = acc + 64 * c;
                 tmem_ld_x32_sync(taddr, r);
-                if (kind == kItemPieceIn)
+                if (add == 1)
                     fused::add_tmem(r, partner_buf + 64 * c);
+                else if (add == 2)
+                    fused::add_slot32(r, piece, row_in_tile, 64 * c);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
                 tmem_ld_x32_sync(taddr + 32, r);
-                if (kind == kItemPieceIn)
+                if (add == 1)
                     fused::add_tmem(r, partner_buf + 64 * c + 32);
+                else if (add == 2)
+                    fused::add_slot32(r, piece, row_in_tile, 64 * c + 32);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
@@ -337,12 +328,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 ++nstores;
             }
+        };
+        for (int64_t i = 0; i < items; ++i) {
+            int64_t t;
+            int kb0, kb1, kind;
+            sk_item_at(sk, pair_id, num_pairs, i, t, kb0, kb1, kind);
+            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
+            const bool ok = wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
+                                         kSiteEpiAccFull);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after_sync();
+            const uint32_t acc = tmem_base + lane_base + buf * BNP;
+            if (kind == kItemPieceOut) {
+                // k tail of a tile cut with the previous pair: publish it; if
+                // that pair's k head was published first, finish the tile here
+                if (p.sk_mode == 2)
+                    fused::sk_test_delay(200000);
+                publish(p.sk_part + (size_t)blockIdx.x * kSlot, acc);
+                if (fused::sk_exchange(tail_cut, fused::sk_tail_tag(p.epoch), lane) ==
+                    fused::sk_head_tag(p.epoch)) {
+                    store_tile(t, acc, 2, prev_head);
+                    __syncwarp();
+                    if (lane == 0)
+                        *tail_cut = 0u;  // consumed
+                }
+            } else if (kind == kItemPieceIn) {
+                // k head of a tile cut with the next pair: add its k tail if
+                // it is there; else publish the head and finish only if the
+                // tail arrived meanwhile
+                int add = preloaded ? 1 : 0;
+                if (!preloaded) {
+                    if (p.sk_mode == 0 &&
+                        fused::sk_peek(head_cut, lane) == fused::sk_tail_tag(p.epoch)) {
+                        add = 2;
+                    } else {
+                        publish(p.sk_head + (size_t)blockIdx.x * kSlot, acc);
+                        add = fused::sk_exchange(head_cut, fused::sk_head_tag(p.epoch), lane) ==
+                                      fused::sk_tail_tag(p.epoch)
+                                  ? 2
+                                  : -1;  // -1: the next pair finishes the tile
+                    }
+                }
+                if (add >= 0) {
+                    store_tile(t, acc, add, next_tail);
+                    if (add == 2) {
+                        __syncwarp();
+                        if (lane == 0)
+                            *head_cut = 0u;  // consumed
+                    }
+                }
+            } else {
+                store_tile(t, acc, 0, nullptr);
+            }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_cluster(acce_leader0 + 8u * buf);
-            if (preload && i == items - 2 && !preload_piece())
-                break;
+            if (head_last && items >= 2 && i == items - 2)
+                try_preload();
         }
         if (lane == 0)
             bulk_wait_group<0>();

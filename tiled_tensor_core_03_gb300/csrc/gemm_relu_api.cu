@@ -44,11 +44,17 @@ std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 12
                                       // 4 GEMV (M <= 8)
 std::atomic<int> g_force_split{0};    // 0 auto, 1 two-stage split-K form only
 std::atomic<int> g_panel_rows{0};     // 0 the default panel, else output rows per panel
+std::atomic<int> g_sk_mode{0};        // stream-K fix-up test mode (0 normal)
 std::atomic<uint32_t> g_epoch{0};
 
+// Stream-K calls are told apart by an epoch below 2^30 (the fix-up tags its
+// state words with epoch * 4 + 1 or + 2), never 0.
 uint32_t next_epoch() {
-    uint32_t e = ++g_epoch;
-    return e ? e : ++g_epoch;
+    for (;;) {
+        const uint32_t e = (++g_epoch) & 0x3fffffffu;
+        if (e)
+            return e;
+    }
 }
 
 // Rasteriser panel height in output rows for a contraction of length K.
@@ -220,9 +226,6 @@ bool ensure_smem_attr(bool &done, Kern kernel, uint32_t bytes) {
 #ifndef GEMMRELU_PDL
 #define GEMMRELU_PDL 1
 #endif
-#ifndef GEMMRELU_SK_COOPERATIVE
-#define GEMMRELU_SK_COOPERATIVE 1
-#endif
 
 // Every kernel of this library is launched through here, with programmatic
 // stream serialisation: it may become resident while the previous grid of
@@ -299,18 +302,17 @@ int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensor
     if (!ensure_smem_attr(attr_done, kern, smem))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
-    // Stream-K: CTAs wait on flags raised by their neighbours, so all of them
-    // must be resident at once -- a cooperative launch guarantees that (or
-    // fails).
+    // (stream-K needs no co-residency: its fix-up never waits for another CTA)
     return launch_kernel(kern, (unsigned)grid, F::Roles<kTma>::kThreads, smem, stream,
-                         GEMMRELU_SK_COOPERATIVE && p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p, rm);
+                         false, 1, mA, mB, mC, p, rm);
 }
 
 // Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
 struct StreamK {
     int64_t dp_tiles = -1;     // -1: plain data-parallel launch
-    float *part = nullptr;
-    uint32_t *flags = nullptr;
+    float *part = nullptr;     // k-tail slots
+    float *head = nullptr;     // k-head slots
+    uint32_t *flags = nullptr; // fix-up state words
     uint32_t epoch = 0;
 };
 
@@ -333,8 +335,10 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
     p.wait_limit_ns = wait_limit_ns();
     p.dp_tiles = sk.dp_tiles >= 0 ? sk.dp_tiles : p.num_tiles;
     p.sk_part = sk.part;
+    p.sk_head = sk.head;
     p.sk_flags = sk.flags;
     p.epoch = sk.epoch;
+    p.sk_mode = g_sk_mode.load();
     CUtensorMap mA, mB, mC;
     if (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
         !make_map(&mC, C, M, N, 64, 32))
@@ -344,7 +348,7 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
     const int64_t pairs = std::min<int64_t>(p.num_tiles, ds->sms / 2);
     // stream-K: pairs wait on flags of their neighbours -> cooperative launch
     return launch_kernel(P::gemm_relu_pair_kernel, (unsigned)(2 * pairs), P::kThreads,
-                         P::kSmemBytes, stream, GEMMRELU_SK_COOPERATIVE && p.dp_tiles != p.num_tiles, 1, mA, mB, mC, p);
+                         P::kSmemBytes, stream, false, 1, mA, mB, mC, p);
 }
 
 // ---------------------------------------------------------------- GEMV (M <= 8)
@@ -469,8 +473,10 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     p.wait_limit_ns = wait_limit_ns();
     p.dp_tiles = sk.dp_tiles >= 0 ? sk.dp_tiles : p.num_tiles;
     p.sk_part = sk.part;
+    p.sk_head = sk.head;
     p.sk_flags = sk.flags;
     p.epoch = sk.epoch;
+    p.sk_mode = g_sk_mode.load();
     CUtensorMap mA, mB, mC;
     std::memset(&mA, 0, sizeof(mA));
     std::memset(&mB, 0, sizeof(mB));
@@ -528,8 +534,9 @@ SkPlan streamk_plan(int64_t M, int64_t N, int sms) {
 }
 
 // Both kernels' slots hold 128 rows x 256 fp32 columns, plus 4 flags.
+constexpr size_t kSkSlotBytes = (size_t)256 * 128 * 4;
 size_t streamk_bytes(int64_t ctas) {
-    return (size_t)ctas * 256 * 128 * 4 + (size_t)ctas * 4 * 4;
+    return 2 * (size_t)ctas * kSkSlotBytes + (size_t)ctas * 4 * 4;
 }
 
 // ---------------------------------------------------------------- split-K
@@ -854,9 +861,10 @@ int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int6
         return GEMMRELU_ERR_WORKSPACE;
     StreamK sk;
     sk.dp_tiles = plan.dp_tiles;
-    sk.part = static_cast<float *>(workspace);
-    sk.flags = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) +
-                                            (size_t)plan.ctas * 256 * 128 * 4);
+    char *ws = static_cast<char *>(workspace);
+    sk.part = reinterpret_cast<float *>(ws);
+    sk.head = reinterpret_cast<float *>(ws + (size_t)plan.ctas * kSkSlotBytes);
+    sk.flags = reinterpret_cast<uint32_t *>(ws + 2 * (size_t)plan.ctas * kSkSlotBytes);
     sk.epoch = next_epoch();
     if (plan.pair)
         return launch_pair(A, B, C, M, N, K, s, ds, sk);
@@ -977,6 +985,13 @@ int gemm_relu_debug_force_split(int which) {
     if (which < 0 || which > 1)
         return GEMMRELU_ERR_INVALID_ARG;
     g_force_split.store(which);
+    return GEMMRELU_OK;
+}
+
+int gemm_relu_debug_streamk(int mode) {
+    if (mode < 0 || mode > 2)
+        return GEMMRELU_ERR_INVALID_ARG;
+    g_sk_mode.store(mode);
     return GEMMRELU_OK;
 }
 

@@ -343,15 +343,17 @@ struct Params {
     // run data-parallel: CTA c takes tiles c, c + G, ...  The k blocks of the
     // remaining tiles are laid end to end and cut into G equal contiguous
     // ranges, one per CTA, so every CTA gets the same amount of MMA work.  A
-    // tile cut between CTA c (its first k blocks, at the end of c's range) and
-    // CTA c + 1 (its last k blocks, at the start of c + 1's range) is summed
-    // through sk_part: c + 1 stores its fp32 piece and raises sk_flags[c + 1],
-    // c adds it to its own piece before the ReLU epilogue.  dp_tiles equal to
-    // num_tiles means no stream-K part.
+    // tile cut between CTA c (its k head: the first k blocks, at the end of
+    // c's range) and CTA c + 1 (its k tail, at the start of c + 1's range) is
+    // finished by whichever of the two gets there second (see sk_exchange):
+    // no CTA ever waits for another.  dp_tiles equal to num_tiles means no
+    // stream-K part.
     int64_t dp_tiles;
-    float *sk_part;        // [G] slots of BM x BN fp32, [BN/4][BM][4] each
-    uint32_t *sk_flags;    // [G][4]: one flag per epilogue warp (32 rows)
-    uint32_t epoch;        // nonzero, distinct per call
+    float *sk_part;        // [G] k-tail slots of BM x BN fp32, [BN/4][BM][4] each
+    float *sk_head;        // [G] k-head slots, same layout
+    uint32_t *sk_flags;    // [G][4]: the state of each cut, one word per epilogue warp
+    uint32_t epoch;        // nonzero, below 2^30, distinct per call
+    int sk_mode;           // test hook: 0 normal; 1 heads always publish; 2 also delay tails
 };
 
 // Tensor maps of the predicated-load kernel: for each residue a modulo 8, the
@@ -434,24 +436,70 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     return v;
 }
 
-// All lanes wait until *f == v (a stream-K piece published by another CTA);
-// bounded like every other wait.
-__device__ __forceinline__ bool wait_flag(const uint32_t *f, uint32_t v, uint64_t limit_ns,
-                                          volatile uint32_t *abort_flag) {
-    if (ld_acquire_gpu(f) == v)
-        return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        __nanosleep(64);
-        if (ld_acquire_gpu(f) == v)
-            return true;
-        if (*abort_flag)
-            return false;
-        if (global_timer_ns() - t0 > limit_ns) {
-            record_timeout(abort_flag, kSitePieceFlag);
-            return false;
-        }
+// Stream-K fix-up of a tile cut between two workers, wait-free.  The state
+// word of the cut (one per epilogue warp) is tagged with the call's epoch:
+// sk_tail_tag when the k tail's fp32 piece is published, sk_head_tag when the
+// k head's is.  Each side publishes its piece only if it may be first, then
+// swaps its tag into the word; the side whose swap returns the other's tag
+// came second and finishes the tile (adds the published piece to its own and
+// stores C).  Exactly one side finishes, neither waits, so the kernels need
+// no co-residency guarantee.  The sum is own + other in fp32, which is the
+// same number whichever side adds (fp32 addition is commutative).
+__device__ __forceinline__ uint32_t sk_tail_tag(uint32_t epoch) { return epoch * 4u + 1u; }
+__device__ __forceinline__ uint32_t sk_head_tag(uint32_t epoch) { return epoch * 4u + 2u; }
+
+// Warp-uniform read of a cut's state: lane 0 loads it with acquire, the warp
+// synchronises, and every lane fences, so every lane's later loads of the
+// other side's piece come after the load that saw its tag.
+__device__ __forceinline__ uint32_t sk_peek(const uint32_t *state, int lane) {
+    uint32_t v = 0;
+    if (lane == 0)
+        v = ld_acquire_gpu(state);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    __syncwarp();
+    __threadfence();
+    return v;
+}
+
+// Warp-uniform swap of `tag` into a cut's state after this warp's piece
+// stores (each lane fences its stores, the warp synchronises, lane 0 fences
+// again -- fences are cumulative -- and swaps); returns the previous state,
+// with the same ordering as sk_peek for the loads that follow.
+__device__ __forceinline__ uint32_t sk_exchange(uint32_t *state, uint32_t tag, int lane) {
+    __threadfence();
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0) {
+        __threadfence();
+        old = atomicExch(state, tag);
+        __threadfence();
     }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    __syncwarp();
+    __threadfence();
+    return old;
+}
+
+// r[j] += column col0 + j of this lane's row of a published piece.
+__device__ __forceinline__ void add_slot32(uint32_t (&r)[32], const float *slot, int row,
+                                           int col0) {
+    const float4 *s = reinterpret_cast<const float4 *>(slot) + (size_t)(col0 / 4) * 128 + row;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = __ldcg(s + (size_t)i * 128);
+        r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + x.x);
+        r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + x.y);
+        r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + x.z);
+        r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + x.w);
+    }
+}
+
+// Test hook: keep a k tail from publishing for about `ns` (bounded by the
+// global timer), so the k head's side of the exchange runs first.
+__device__ __forceinline__ void sk_test_delay(uint64_t ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns)
+        __nanosleep(1000);
 }
 
 // r[j] += the 32 fp32 columns at TMEM address taddr (this lane's row).
@@ -835,75 +883,43 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         // ============================================================ epilogue
         const int ew = warp - R::kEpiWarp0;     // staging buffer owner 0..3
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
+        const int row_in_tile = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * 2u * kEpiBuf;
         uint32_t nstores = 0;
         const int64_t items = num_items(p, blockIdx.x, gridDim.x);
-        // Stream-K: when the last item is a k head piece, the next CTA's
-        // published k tail is copied into the other TMEM accumulator buffer
-        // once the item before the k head has been read (that buffer is not
-        // used again), while the MMA works on the k head; the k head's
-        // epilogue then adds the two buffers.  The MMA never waits for it, and
-        // this CTA has published its own k tail (its first stream-K item)
-        // before it waits for its neighbour's, so waits cannot chain.
+        // Stream-K (TMA path only).  This CTA holds the k tail of the tile cut
+        // with the previous CTA (its first stream-K item) and the k head of
+        // the tile cut with the next one (its last item).  When the k head is
+        // last and the next CTA's k tail is already published by the time the
+        // item before the k head has been read, the tail is copied into the
+        // other TMEM buffer (not used again) while the MMA works on the head,
+        // and the head's epilogue adds the two buffers; otherwise the two
+        // sides meet through sk_exchange.
         int64_t last_t = 0;
         int last_kb0 = 0, last_kb1 = 0, last_kind = kItemFull;
         if (items > 0)
             item_at(p, blockIdx.x, gridDim.x, items - 1, last_t, last_kb0, last_kb1, last_kind);
-        // (stream-K runs on the TMA path only)
-        const bool preload = kTma && last_kind == kItemPieceIn && items >= 2;
+        const bool head_last = kTma && last_kind == kItemPieceIn;
         const uint32_t partner_buf = tmem_base + lane_base + (uint32_t)((items - 2) & 1) * BN;
-        auto preload_piece = [&]() -> bool {
-            uint32_t *flag = p.sk_flags + (blockIdx.x + 1) * 4 + q;
-            const bool got = wait_flag(flag, p.epoch, p.wait_limit_ns, abort_flag);
-            if (!__all_sync(0xffffffffu, got))
-                return false;
-            piece_to_tmem<BN>(p.sk_part + (size_t)(blockIdx.x + 1) * BN * BM, 32 * q + lane,
-                              partner_buf);
+        uint32_t *const head_cut = p.sk_flags + (blockIdx.x + 1) * 4 + q;  // this CTA's k head
+        uint32_t *const tail_cut = p.sk_flags + blockIdx.x * 4 + q;        // this CTA's k tail
+        const float *const next_tail = p.sk_part + (size_t)(blockIdx.x + 1) * BN * BM;
+        const float *const prev_head =
+            blockIdx.x > 0 ? p.sk_head + (size_t)(blockIdx.x - 1) * BN * BM : nullptr;
+        bool preloaded = false;
+        auto try_preload = [&]() {
+            if (p.sk_mode != 0 || sk_peek(head_cut, lane) != sk_tail_tag(p.epoch))
+                return;
+            piece_to_tmem<BN>(next_tail, row_in_tile, partner_buf);
             __syncwarp();
             if (lane == 0)
-                *flag = 0u;  // consumed: no later call can mistake it for its own
-            return true;
+                *head_cut = 0u;  // consumed
+            preloaded = true;
         };
-        bool alive = true;
-        for (int64_t i = 0; alive && i < items; ++i) {
-            int64_t t;
-            int kb0, kb1, kind;
-            item_at(p, blockIdx.x, gridDim.x, i, t, kb0, kb1, kind);
-            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
-            // (the predicated-load kernel's producers share the schedulers
-            // with these warps: poll slowly there)
-            const bool ok = kTma ? wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
-                                                kSiteEpiAccFull)
-                                 : wait_bounded_sleep(accf_bar(buf), use, p.wait_limit_ns,
-                                                      abort_flag, kSiteEpiAccFull, 256);
-            if (!__all_sync(0xffffffffu, ok))
-                break;
-            tc_fence_after_sync();
-            const uint32_t acc = tmem_base + lane_base + buf * BN;
-            const bool preload_next = preload && i == items - 2;
-            if (kTma && kind == kItemPieceOut) {
-                // k tail of a tile cut with the previous CTA: publish the raw
-                // fp32 piece in this CTA's slot.
-                float *slot = p.sk_part + (size_t)blockIdx.x * BN * BM;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_x32_sync(acc + 32 * c, r);
-                    piece_store32(slot, 32 * q + lane, 32 * c, r);
-                }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0)
-                    st_release_gpu(p.sk_flags + blockIdx.x * 4 + q, p.epoch);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(acce_bar(buf));
-                if (preload_next && !preload_piece())
-                    break;
-                continue;
-            }
+        // Stores tile t from accumulator `acc` (+ the TMEM partner buffer
+        // when add == 1, + a published piece when add == 2) as ReLU'd fp16.
+        auto store_tile = [&](int64_t t, uint32_t acc, int add, const float *piece) {
             int64_t mb, nb;
             tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
             const int64_t row0 = mb * BM + 32 * q;
@@ -916,14 +932,18 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 uint32_t r[32], h[32];
                 const uint32_t taddr = acc + 64 * c;
                 tmem_ld_x32_sync(taddr, r);
-                if (kTma && kind == kItemPieceIn)
+                if (kTma && add == 1)
                     add_tmem(r, partner_buf + 64 * c);
+                if (kTma && add == 2)
+                    add_slot32(r, piece, row_in_tile, 64 * c);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
                 tmem_ld_x32_sync(taddr + 32, r);
-                if (kTma && kind == kItemPieceIn)
+                if (kTma && add == 1)
                     add_tmem(r, partner_buf + 64 * c + 32);
+                if (kTma && add == 2)
+                    add_slot32(r, piece, row_in_tile, 64 * c + 32);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
@@ -975,13 +995,78 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     __syncwarp();
                 }
             }
+        };
+        // Publishes this lane's row of accumulator `acc` into `slot`.
+        auto publish = [&](float *slot, uint32_t acc) {
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_x32_sync(acc + 32 * c, r);
+                piece_store32(slot, row_in_tile, 32 * c, r);
+            }
+        };
+        for (int64_t i = 0; i < items; ++i) {
+            int64_t t;
+            int kb0, kb1, kind;
+            item_at(p, blockIdx.x, gridDim.x, i, t, kb0, kb1, kind);
+            const uint32_t buf = (uint32_t)(i & 1), use = (uint32_t)((i >> 1) & 1);
+            // (the predicated-load kernel's producers share the schedulers
+            // with these warps: poll slowly there)
+            const bool ok = kTma ? wait_bounded(accf_bar(buf), use, p.wait_limit_ns, abort_flag,
+                                                kSiteEpiAccFull)
+                                 : wait_bounded_sleep(accf_bar(buf), use, p.wait_limit_ns,
+                                                      abort_flag, kSiteEpiAccFull, 256);
+            if (!__all_sync(0xffffffffu, ok))
+                break;
+            tc_fence_after_sync();
+            const uint32_t acc = tmem_base + lane_base + buf * BN;
+            if (kTma && kind == kItemPieceOut) {
+                // k tail of a tile cut with the previous CTA: publish it; if
+                // that CTA's k head was published first, finish the tile here.
+                if (p.sk_mode == 2)
+                    sk_test_delay(200000);
+                publish(p.sk_part + (size_t)blockIdx.x * BN * BM, acc);
+                if (sk_exchange(tail_cut, sk_tail_tag(p.epoch), lane) == sk_head_tag(p.epoch)) {
+                    store_tile(t, acc, 2, prev_head);
+                    __syncwarp();
+                    if (lane == 0)
+                        *tail_cut = 0u;  // consumed
+                }
+            } else if (kTma && kind == kItemPieceIn) {
+                // k head of a tile cut with the next CTA: add its k tail if it
+                // is there; else publish the head, and finish only if the tail
+                // arrived meanwhile.
+                int add = preloaded ? 1 : 0;
+                if (!preloaded) {
+                    if (p.sk_mode == 0 && sk_peek(head_cut, lane) == sk_tail_tag(p.epoch)) {
+                        add = 2;
+                    } else {
+                        publish(p.sk_head + (size_t)blockIdx.x * BN * BM, acc);
+                        if (sk_exchange(head_cut, sk_head_tag(p.epoch), lane) ==
+                            sk_tail_tag(p.epoch))
+                            add = 2;
+                        else
+                            add = -1;  // the next CTA finishes the tile
+                    }
+                }
+                if (add >= 0) {
+                    store_tile(t, acc, add, next_tail);
+                    if (add == 2) {
+                        __syncwarp();
+                        if (lane == 0)
+                            *head_cut = 0u;  // consumed
+                    }
+                }
+            } else {
+                store_tile(t, acc, 0, nullptr);
+            }
             // accumulator buffer fully read: hand it back to the MMA warp
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acce_bar(buf));
-            if (preload_next && !preload_piece())
-                break;
+            if (head_last && items >= 2 && i == items - 2)
+                try_preload();
         }
         if constexpr (kTma) {
             if (lane == 0)
