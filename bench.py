@@ -48,6 +48,7 @@ INPUT_SETS = 3                   # operand copies each headline part rotates thr
 ROTATE_BYTES = 256 << 20         # small workloads rotate through at least this many operand bytes
 PART_LOOP_S = 1.0                # per-part loops run at least this long (clock samples)
 HOLD_S = 2e-3                    # GPU-side hold before a timed region (the host queues ahead)
+COOL_S = 0.5                     # idle before each per-part measurement
 SOAK_S = 1.2                     # clock soak of the step
 
 METRIC = "GEMM+ReLU TFLOP/s (fp16 in, fp32 acc)"
@@ -728,7 +729,7 @@ def measure_step(gpu, args, world, parts, name):
     # events only at the two ends (an event recorded between two launches
     # serialises them and would add its own cost to the step)
     sampler = gpu.sampler
-    time.sleep(0.3)
+    time.sleep(COOL_S)
     e_start, e_end = gpu.events()
     barrier(world)
     gpu.sync()
@@ -758,6 +759,9 @@ def measure_step(gpu, args, world, parts, name):
     # peak)
     part_ms, sustained = {}, {}
     for label, w, kind in parts:
+        # each part from the same idle state: right after another part's
+        # power-capped loop the clocks take a while to come back up
+        time.sleep(COOL_S)
         part_ms[label] = gpu.time_stream(launch[label], INPUT_SETS, args.steps)
         ms, n, clk = gpu.time_loop(launch[label], INPUT_SETS, PART_LOOP_S, part_ms[label])
         sustained[label] = {"ms": ms, "launches": n, "clocks": clk,
@@ -765,7 +769,10 @@ def measure_step(gpu, args, world, parts, name):
                             "gbs": w.bytes / (ms * 1e-3) / 1e9}
     # ---- warm: each part alone, back to back on the same operands (L2 may
     # hold them: the 4096^3 operands fit, the skinny B is about L2's size)
-    warm_ms = {label: gpu.time_stream(launch[label], 1, args.steps) for label, _, _ in parts}
+    warm_ms = {}
+    for label, _, _ in parts:
+        time.sleep(COOL_S)
+        warm_ms[label] = gpu.time_stream(launch[label], 1, args.steps)
     check_status(gr, stream, "after the per-part loops")
     # ---- cold launches: L2 flushed before each, events around each alone
     cold_ms = {label: gpu.time_cold(launch[label], max(3, min(args.steps, 10)))
@@ -862,7 +869,7 @@ def measure_step(gpu, args, world, parts, name):
                       "hold recorded before the start event (the host's launch latency after "
                       "an idle spell stays out of the region); value and ms_per_step from CUDA "
                       "events at the two ends of the timed region only; parts (and roofline): "
-                      "each part alone, K launches back to back on the rotating input sets, "
+                      "each part alone after 0.5 s idle, K launches back to back on the rotating input sets, "
                       f"events at both ends; parts.sustained: the same for at least "
                       f"{PART_LOOP_S:.0f} s with the clocks sampled (power cap), against the "
                       f"sustained peak; cold_launch: L2 flushed, "

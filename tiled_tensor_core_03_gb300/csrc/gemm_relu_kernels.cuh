@@ -298,17 +298,19 @@ constexpr int kEpiWarps = 4;
 
 // Per tile width BN (UMMA N = TMEM columns per accumulator): 256 or 128.
 // The TMA kernels' ring gets as many stages as fit beside 32 KB of epilogue
-// staging.  The predicated-load kernel (kTma false, BN = 128) keeps two
-// operand stages and, before them, a ring of kRawStages raw stages: the
-// aligned 16-byte blocks of each row segment as TMA brings them (A: 128 rows
-// of 9 blocks, B: 64 k-rows of 17 blocks, grouped by row residue modulo 8),
-// which its producers shift into the operand layout.
+// staging (two buffers per epilogue warp).  The predicated-load kernel
+// (kTma false, BN = 128) keeps two operand stages and, before them, a ring of
+// kRawStages raw stages: the aligned 16-byte blocks of each row segment as
+// TMA brings them (A: 128 rows of 9 blocks, B: 64 k-rows of 17 blocks,
+// grouped by row residue modulo 8), which its producers shift into the
+// operand layout; its epilogue stores from one staging buffer per warp.
 template <int kBN, bool kTma = true>
 struct Tile {
     static constexpr int BN = kBN;
     static constexpr uint32_t kBTile = BK * BN * 2;          // BN / 64 slabs, MN-major
     static constexpr int kStages = kTma ? (kBN >= 256 ? 4 : 6) : 2;
     static constexpr int kRawStages = kTma ? 0 : 3;
+    static constexpr int kEpiBufs = kTma ? 2 : 1;            // staging buffers per epilogue warp
     static constexpr uint32_t kRawRowA = (BK / 8 + 1) * 16;  // 144 B
     static constexpr uint32_t kRawRowB = (BN / 8 + 1) * 16;  // 272 B at BN = 128
     static constexpr uint32_t kRawB = BM * kRawRowA;         // B rows follow the A rows
@@ -318,7 +320,7 @@ struct Tile {
     static constexpr uint32_t kOffB = kOffA + kStages * kATile;
     static constexpr uint32_t kOffRaw = kOffB + kStages * kBTile;
     static constexpr uint32_t kOffEpi = kOffRaw + kRawStages * kRawStage;
-    static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBuf;
+    static constexpr uint32_t kOffBar = kOffEpi + kEpiWarps * kEpiBufs * kEpiBuf;
     static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1 + 8 * kRawStages;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemUsed = kOffMisc + 16;
@@ -885,7 +887,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31
         const int row_in_tile = 32 * q + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * 2u * kEpiBuf;
+        const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * T::kEpiBufs * kEpiBuf;
         uint32_t nstores = 0;
         const int64_t items = num_items(p, blockIdx.x, gridDim.x);
         // Stream-K (TMA path only).  This CTA holds the k tail of the tile cut
