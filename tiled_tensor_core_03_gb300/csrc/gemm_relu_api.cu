@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <random>
 #include <utility>
 
 #include "gemm_relu.h"
@@ -45,10 +46,14 @@ std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 12
 std::atomic<int> g_force_split{0};    // 0 auto, 1 two-stage split-K form only
 std::atomic<int> g_panel_rows{0};     // 0 the default panel, else output rows per panel
 std::atomic<int> g_sk_mode{0};        // stream-K fix-up test mode (0 normal)
-std::atomic<uint32_t> g_epoch{0};
+// Starts from a value drawn per process, so that state words a stream-K call
+// of another process left behind in reused device memory are unlikely to
+// carry the tag of one of this process's calls.
+std::atomic<uint32_t> g_epoch{(uint32_t)std::random_device{}()};
 
 // Stream-K calls are told apart by an epoch below 2^30 (the fix-up tags its
-// state words with epoch * 4 + 1 or + 2), never 0.
+// state words with epoch * 4 + 1 or + 2), never 0; the side that finishes a
+// cut tile resets its state word to 0.
 uint32_t next_epoch() {
     for (;;) {
         const uint32_t e = (++g_epoch) & 0x3fffffffu;
