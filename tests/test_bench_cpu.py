@@ -84,3 +84,25 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     ns.workload = "attn"
     assert bench.run_reference_attention(ns, 2, 1) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_traffic_hash_covers_every_kernel_source():
+    """Every CUDA source of the library is in the hash that keys the stored
+    DRAM traffic figures, so no kernel can change without voiding them."""
+    csrc = os.path.join(ROOT, "tiled_tensor_core_03_gb300", "csrc")
+    sources = {f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))}
+    assert sources == set(bench.KERNEL_SOURCES)
+
+
+def test_traffic_reported_only_for_the_captured_sources(monkeypatch):
+    key = next(iter(bench.TRAFFIC_CAPTURE["bytes"]))
+    cur = bench.kernel_source_hash()
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURE, "source_hash", cur)
+    value, note = bench.traffic_for(key)
+    assert value == bench.TRAFFIC_CAPTURE["bytes"][key] and cur in note
+    assert bench.traffic_for(("fused", 3, 5, 7))[0] is None           # shape never captured
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURE, "source_hash", "0" * 16)
+    value, note = bench.traffic_for(key)
+    assert value is None and "changed" in note
+    monkeypatch.setitem(bench.TRAFFIC_CAPTURE, "source_hash", None)
+    assert bench.traffic_for(key)[0] is None
