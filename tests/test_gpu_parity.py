@@ -368,6 +368,33 @@ def test_streamk_fixup_orders_give_identical_bits(orc, sk_kernel, M, N, K):
         _sampled_parity(orc, A, B, host(c), (M, N, K, "fix-up mode", mode))
 
 
+def test_streamk_concurrent_streams(sk_kernel):
+    """Stream-K launches on two streams at once (distinct workspaces), beside
+    a long library kernel of another stream that holds SMs meanwhile: no
+    worker ever waits for another, so every launch completes with the same
+    bits as when it runs alone."""
+    import torch
+    M, N, K = 2048, 5120, 320
+    A, B = inputs.make(M, N, K, "normal", True, seed=99)
+    a, b = dev(A), dev(B)
+    alone = gr.gemm_relu_streamk(a, b, workspace=gr.streamk_workspace(M, N, K))
+    big_a = torch.randn(8192, 8192, device="cuda").half()
+    s1, s2, s3 = (torch.cuda.Stream() for _ in range(3))
+    # every buffer stays referenced until the end: the caching allocator
+    # knows only the current stream, not the streams the kernels run on
+    keep = [gr.streamk_workspace(M, N, K) for _ in range(8)]
+    outs = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in range(8)]
+    big_c = torch.empty_like(big_a)
+    torch.cuda.synchronize()
+    gr.gemm_relu(big_a, big_a, out=big_c, stream=s3)   # ~0.6 ms on all SMs
+    for i in range(8):
+        gr.gemm_relu_streamk(a, b, out=outs[i], workspace=keep[i], stream=(s1, s2)[i % 2])
+    torch.cuda.synchronize()
+    assert gr.status() == gr.OK
+    for c in outs:
+        assert torch.equal(c.view(torch.int16), alone.view(torch.int16))
+
+
 def test_streamk_falls_back_without_a_cut():
     import torch
     # 1024 x 2048 x 512: 32 tiles, fewer than the SMs -> plain kernel, no workspace
