@@ -448,7 +448,8 @@ def test_panel_height_changes_only_the_tile_order(forced_kernel):
     summed in two parts): each height is deterministic and within the
     contract of the plain result."""
     import torch
-    for (M, N, K) in [(2304, 1792, 384), (1664, 2560, 200)]:
+    for (M, N, K) in [(2304, 1792, 384), (1664, 2560, 200), (2305, 1031, 333)]:
+        # (the last: odd row pitches, the predicated-load kernel)
         A, B = inputs.make(M, N, K, seed=M + K)
         a, b = dev(A), dev(B)
         ws = gr.streamk_workspace(M, N, K)
