@@ -121,3 +121,22 @@ def test_attention_dropped_arrival_times_out_and_recovers(orc):
     out = host(gr.flash_attention(q, k, v, causal=True))
     assert gr.status() == gr.OK
     _check(orc, out, Q, K, V, True)
+
+
+def _attention_shapes(seed, n):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 3)), int(rng.integers(1, 700)), int(rng.integers(1, 4)),
+             int(rng.choice([64, 128])), bool(rng.integers(0, 2)), float(rng.choice([0.5, 1.0, 1.5])))
+            for _ in range(n)]
+
+
+@pytest.mark.parametrize("chunk", range(3))
+def test_attention_random_shapes(orc, chunk):
+    """Seeded random batch, sequence length (1 to ~700: partial key blocks,
+    a padding tile when the tiles are odd), heads, head size, causal flag and
+    score scale, against the oracle with the contract and the rounding bound."""
+    for (b, s, h, d, causal, sc) in _attention_shapes(500 + chunk, 8):
+        Q, K, V = _inputs(b, s, h, d, seed=b * 7 + s * 3 + h + d, scale=sc)
+        out = host(gr.flash_attention(dev(Q), dev(K), dev(V), causal=causal))
+        assert gr.status() == gr.OK, (b, s, h, d, causal)
+        _check(orc, out, Q, K, V, causal)
