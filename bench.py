@@ -60,7 +60,8 @@ KERNEL_CHOICES = {"auto": 0, "one_cta_256": 1, "one_cta_128": 2, "pair": 3, "gem
 # ------------------------------------------------------------------ DRAM traffic
 
 KERNEL_SOURCES = ("gemm_relu_api.cu", "gemm_relu_kernels.cuh", "gemm_relu_splitk.cuh",
-                  "gemm_relu_2sm.cuh", "gemm_relu_gemv.cuh", "flash_attention.cuh", "sm103.cuh")
+                  "gemm_relu_2sm.cuh", "gemm_relu_gemv.cuh", "flash_attention.cuh", "sm103.cuh",
+                  "gemm_relu_stage.cuh")
 
 
 def kernel_source_hash():
@@ -943,12 +944,15 @@ def measure_step(gpu, args, world, parts, name):
 # ------------------------------------------------------------------ one GEMM workload
 
 def measure_config(gpu, w, steps, warmup, world, cpu_budget, want_cpu=True):
-    """One GEMM workload through gemm_relu: device time by CUDA-graph replay
-    over enough rotating operand copies that every launch reads operands
-    last touched at least ROTATE_BYTES of other operands earlier; plain
-    back-to-back launches (with the host's per-call cost), cold launches, the
-    end-to-end leg, the CPU oracle on all host cores (and on one core for the
-    two square shapes) and a full-output parity check against it."""
+    """One GEMM workload through gemm_relu_streamk (the library's call with a
+    workspace: a stream-K schedule where one applies, operands whose rows TMA
+    cannot describe copied into aligned rows first, else gemm_relu_f16's
+    kernel): device time by CUDA-graph replay over enough rotating operand
+    copies that every launch reads operands last touched at least
+    ROTATE_BYTES of other operands earlier; plain back-to-back launches (with
+    the host's per-call cost), cold launches, the end-to-end leg, the CPU
+    oracle on all host cores (and on one core for the two square shapes) and
+    a full-output parity check against it."""
     import torch
     import tiled_tensor_core_03_gb300 as gr
     from tiled_tensor_core_03_gb300 import inputs
@@ -963,10 +967,13 @@ def measure_config(gpu, w, steps, warmup, world, cpu_budget, want_cpu=True):
     del a_dev, b_dev
     path = gr.gemm_relu_f16_path(sets[0][0].data_ptr(), sets[0][1].data_ptr(),
                                  sets[0][2].data_ptr(), w.M, w.N, w.K)
+    # one workspace: the launches of a stream run one after another
+    ws_bytes = gr.gemm_relu_f16_streamk_workspace_bytes(w.M, w.N, w.K)
+    ws = gr.streamk_workspace(w.M, w.N, w.K, device)
 
     def launch(r, s):
         a, b, c = sets[r]
-        gr.gemm_relu(a, b, out=c, stream=s)
+        gr.gemm_relu_streamk(a, b, out=c, workspace=ws, stream=s)
 
     for i in range(max(3, warmup)):
         launch(i % nsets, gpu.stream)
@@ -986,19 +993,25 @@ def measure_config(gpu, w, steps, warmup, world, cpu_budget, want_cpu=True):
                        lambda r: [(hC, sets[r][2])])], max(steps, 20), max(3, warmup), world)
     check_status(gr, gpu.stream, f"after the end-to-end leg of {w.name}")
 
+    launches_per_call = 1
     if path == 1:
         kern = ("GEMV kernel" if w.M <= 2 else
                 "CTA-pair kernel (256 x 256 tiles)" if w.M >= 256 and w.N >= 256 else
                 "single-CTA fused kernel")
+        if ws_bytes > 0:
+            kern += ", stream-K schedule"
     else:
-        kern = "predicated-load fused kernel (row pitches not multiples of 16 B)"
+        kern = ("copy kernel for the operands whose row pitch is not a multiple of 16 B "
+                f"({ws_bytes / 2**20:.1f} MiB of workspace), then the single-CTA TMA kernel "
+                "with predicated stores of C")
+        launches_per_call = 2
     out = {
         "workload": describe(w),
-        "kernel": f"gemm_relu_f16 {w.M}x{w.N}x{w.K}: {kern}, as the library selects",
+        "kernel": f"gemm_relu_f16_streamk {w.M}x{w.N}x{w.K}: {kern}, as the library selects",
         "path": {1: "tma", 2: "predicated"}.get(path, str(path)),
         "ms": ms, "tflops": w.flops / (ms * 1e-3) / 1e12, "gbs": w.bytes / (ms * 1e-3) / 1e9,
-        "roofline": gpu.roofline(f"gemm_relu_f16 {w.M}x{w.N}x{w.K} ({kern})", w.flops, w.bytes, ms,
-                                 ("fused", w.M, w.N, w.K)),
+        "roofline": gpu.roofline(f"gemm_relu_f16_streamk {w.M}x{w.N}x{w.K} ({kern})", w.flops,
+                                 w.bytes, ms, ("fused", w.M, w.N, w.K)),
         "timing": (f"CUDA graph of {reps} launches rotating {nsets} operand copies "
                    f"({nsets * w.bytes / 2**20:.0f} MiB: inputs larger than L2), replayed 3 times "
                    f"with events around each replay, median; stream_ms: plain launches back to "
@@ -1009,8 +1022,8 @@ def measure_config(gpu, w, steps, warmup, world, cpu_budget, want_cpu=True):
         "e2e": {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": 2 * (w.M * w.K + w.K * w.N),
                 "d2h_bytes_per_step": 2 * w.M * w.N,
-                "api": "tiled_tensor_core_03_gb300.gemm_relu from pinned host buffers; upload, "
-                       "kernel and read-back on three streams"},
+                "api": "tiled_tensor_core_03_gb300.gemm_relu_streamk from pinned host buffers; "
+                       "upload, kernel and read-back on three streams"},
     }
     if want_cpu:
         import multiprocessing
@@ -1029,7 +1042,7 @@ def measure_config(gpu, w, steps, warmup, world, cpu_budget, want_cpu=True):
                                              f"({f1 / 1e9:.3f} GFLOP in {dt1:.2f} s), one thread"}
         out["cpu_baseline"] = cb
         out["parity"] = dict(contract_check(got[:rows], want), rows_checked=rows)
-    out["gpu_launches"] = reps
+    out["gpu_launches"] = reps * launches_per_call
     return out
 
 

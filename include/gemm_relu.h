@@ -85,35 +85,55 @@ int gemm_relu_f16(const void *A, const void *B, void *C,
 /*
  * gemm_relu_f16_streamk_workspace_bytes -- bytes of device workspace that
  * gemm_relu_f16_streamk needs for these sizes on the current device (its SM
- * count decides the schedule); 0 when the call would run no stream-K part,
- * for invalid arguments, or when no CUDA device is available.
+ * count decides the schedule): when K or N is not a multiple of 8, room for
+ * aligned copies of A and B; otherwise the stream-K schedule's, 0 when the
+ * call would run no stream-K part.  0 for invalid arguments, or when no CUDA
+ * device is available.
  */
 size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 /*
  * gemm_relu_f16_streamk -- C = fp16(max(A . B, 0)) like gemm_relu_f16, with a
- * stream-K schedule for the tiles of the last, partial wave.
+ * stream-K schedule for the tiles of a partial wave, and operands whose rows
+ * TMA cannot describe copied once into aligned rows of the workspace.
  *
  * "TileLang tutorial" (chapter "Persistent kernel") names the problem: when
  * the number of output tiles is not a multiple of the number of SMs, the
  * last wave runs on part of the GPU only; stream-K splits the remaining work
  * over all CTAs along K.  Here all full waves but the last run data-parallel
- * (one 128 x 256 tile per CTA at a time); the k blocks of the remaining
- * tiles are divided into one equal contiguous range per CTA.  A tile cut
- * between two CTAs is summed as (first k blocks) + (last k blocks) in fp32
- * before the ReLU and the fp16 store, by whichever of the two CTAs finishes
- * its part second: each publishes its fp32 piece through `workspace` unless
- * the other's is already there, and neither ever waits for the other, so
- * the kernel needs no guarantee that its CTAs run at the same time.  Each
- * tile is cut at most once and fp32 addition is commutative, so the result
- * is the same from run to run.
+ * (one 128 x 256 tile per CTA, or per CTA pair, at a time); the k blocks of
+ * the remaining tiles are divided into one equal contiguous range per
+ * worker.  With fewer single-CTA tiles than SMs and a long K (M > 64, when
+ * the ranges come out at least 32 k blocks shorter than a tile and the
+ * operand that several tiles share fits in half of L2), all tiles are spread
+ * this way over up to two CTAs per tile.  A tile cut between workers is
+ * summed in fp32 before the ReLU and the fp16 store: each cut is settled by
+ * whichever of its two sides gets there second, each side publishing its
+ * fp32 part through `workspace` unless the other's is already there, and no
+ * CTA ever waits for another, so the kernel needs no guarantee that its CTAs
+ * run at the same time.  A tile cut more than once is summed from its last
+ * k blocks backwards, p0 + (p1 + (p2 + ...)) over its pieces in k order,
+ * whatever the order of arrival (fp32 addition is commutative), so the
+ * result is the same from run to run.
+ *
+ * Operands: when A's or B's rows do not start on 16-byte boundaries (a row
+ * pitch that is not a multiple of 8 elements, or an unaligned base), the
+ * call first copies that operand into rows of pitch round_up(cols, 8) in
+ * the workspace (one extra kernel), then runs the TMA kernel on the copy;
+ * when C's rows are unaligned, the kernel stores C with predicated stores.
+ * The result has the same bits as gemm_relu_f16's predicated-load kernel.
  *
  * workspace: device buffer of at least
  *            gemm_relu_f16_streamk_workspace_bytes(M, N, K) bytes, 16-byte
  *            aligned; its contents need no initialisation.  Calls that may
  *            run concurrently on the GPU must use distinct workspaces.
- * When the tiles already fill whole waves, or the operands cannot use TMA,
- * the call runs gemm_relu_f16's kernel and leaves the workspace untouched.
+ *            Returns GEMMRELU_ERR_WORKSPACE when it is needed and missing,
+ *            smaller than that or misaligned.  With aligned pitches but an
+ *            unaligned base, the copies are made when the workspace has room
+ *            for them, else gemm_relu_f16's predicated-load kernel runs.
+ * When the tiles already fill whole waves and the operands' rows are
+ * aligned, the call runs gemm_relu_f16's kernel and leaves the workspace
+ * untouched.
  */
 int gemm_relu_f16_streamk(const void *A, const void *B, void *C,
                           int64_t M, int64_t N, int64_t K,
@@ -288,16 +308,29 @@ int gemm_relu_debug_set_panel(int rows);
 
 /*
  * gemm_relu_debug_streamk -- test hook for the stream-K fix-up of a tile cut
- * between two workers.  0 (default): the side that holds the tile's first k
- * blocks adds the other side's published piece when it is already there.
+ * between two workers.  0 (default): the side that holds the k blocks left
+ * of the cut adds the other side's published piece when it is already there.
  * 1: that side always publishes its own piece first, so the second side to
- * arrive finishes the tile from global memory.  2: as 1, and the side that
- * holds the last k blocks also waits about 0.2 ms before publishing, so the
- * other order of arrival is exercised.  All modes give the same bits.
+ * arrive finishes the cut from global memory.  2: as 1, and the side right of
+ * the cut also waits about 0.2 ms before publishing.  3: as 1, and the side
+ * left of the cut waits about 0.2 ms instead.  Modes 2 and 3 exercise the
+ * two orders of arrival (and, for a tile cut more than once, which worker
+ * carries the sum on to the next cut).  All modes give the same bits.
  * Affects the calling process only.  Returns GEMMRELU_OK, or
  * GEMMRELU_ERR_INVALID_ARG for another value.
  */
 int gemm_relu_debug_streamk(int mode);
+
+/*
+ * gemm_relu_debug_streamk_pieces -- test hook.  The number of pieces each
+ * tile's k blocks are cut into by gemm_relu_f16_streamk's sub-wave schedule
+ * (fewer single-CTA tiles than SMs): 2 .. 8, or 0 for the library's choice
+ * (default; 2, each tile cut once in the middle).  With 3 or more, tiles
+ * have middle pieces and are settled through chains of cuts.  Affects the
+ * calling process only.  Returns GEMMRELU_OK, or GEMMRELU_ERR_INVALID_ARG
+ * for another value.
+ */
+int gemm_relu_debug_streamk_pieces(int pieces);
 
 #ifdef __cplusplus
 }

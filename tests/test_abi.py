@@ -48,10 +48,14 @@ def test_strerror(lib):
 
 
 def test_streamk_hook_arguments(lib):
-    assert gr.gemm_relu_debug_streamk(3) == gr.ERR_INVALID_ARG
+    assert gr.gemm_relu_debug_streamk(4) == gr.ERR_INVALID_ARG
     assert gr.gemm_relu_debug_streamk(-1) == gr.ERR_INVALID_ARG
-    for mode in (gr.SK_TAIL_LATE, gr.SK_HEAD_PUBLISHES, gr.SK_NORMAL):
+    for mode in (gr.SK_HEAD_LATE, gr.SK_TAIL_LATE, gr.SK_HEAD_PUBLISHES, gr.SK_NORMAL):
         assert gr.gemm_relu_debug_streamk(mode) == gr.OK
+    for bad in (1, 9, -1):
+        assert gr.gemm_relu_debug_streamk_pieces(bad) == gr.ERR_INVALID_ARG
+    for ok in (8, 3, 2, 0):
+        assert gr.gemm_relu_debug_streamk_pieces(ok) == gr.OK
 
 
 def test_panel_hook_arguments(lib):

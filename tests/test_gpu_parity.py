@@ -395,9 +395,162 @@ def test_streamk_concurrent_streams(sk_kernel):
         assert torch.equal(c.view(torch.int16), alone.view(torch.int16))
 
 
+# Shapes whose stream-K schedule is sub-wave (fewer single-CTA tiles than SMs,
+# long K), with the pieces per tile (0: the library's choice).  Two pieces cut
+# each tile once; more give every tile middle pieces, settled through chains
+# of cuts.
+SUBWAVE_CASES = [
+    (200, 3000, 4096, 0),    # 48 tiles of 64 k blocks: 2 pieces on 96 CTAs
+    (128, 2048, 16384, 0),   # 16 tiles of 256 k blocks: 3 pieces on 48 CTAs
+    (128, 4096, 8192, 4),    # 32 tiles of 128 k blocks: 4 pieces on 128 CTAs
+]
+
+
+@pytest.mark.parametrize("M,N,K,pieces", SUBWAVE_CASES)
+def test_streamk_subwave_parity_and_fixup_orders(orc, M, N, K, pieces):
+    """Every element against the oracle, and the same bits in every fix-up
+    order: heads adding a published tail, heads always publishing, tails
+    late (the rightmost worker of a tile carries the sum through each cut)
+    and heads late (the workers left of each cut finish)."""
+    import torch
+    A, B = inputs.make(M, N, K, "normal", True, seed=M + 3 * N + K)
+    a, b = dev(A), dev(B)
+    outs = []
+    try:
+        assert gr.gemm_relu_debug_streamk_pieces(pieces) == gr.OK
+        assert gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K) > 0, "no stream-K part"
+        ws = gr.streamk_workspace(M, N, K)
+        for mode in (gr.SK_NORMAL, gr.SK_HEAD_PUBLISHES, gr.SK_TAIL_LATE, gr.SK_HEAD_LATE,
+                     gr.SK_NORMAL):
+            assert gr.gemm_relu_debug_streamk(mode) == gr.OK
+            ws.random_(0, 256)                      # contents need no initialisation
+            outs.append((mode, gr.gemm_relu_streamk(a, b, workspace=ws)))
+            assert gr.status() == gr.OK
+    finally:
+        gr.gemm_relu_debug_streamk(gr.SK_NORMAL)
+        gr.gemm_relu_debug_streamk_pieces(0)
+    want = oracle_threaded(orc, A, B)
+    assert_parity(host(outs[0][1]), want, abs_dot(A, B), K, (M, N, K, pieces, "stream-K"))
+    for mode, c in outs[1:]:
+        assert torch.equal(c.view(torch.int16), outs[0][1].view(torch.int16)), (M, N, K, mode)
+
+
+def test_streamk_subwave_on_every_single_cta_width():
+    """The sub-wave schedule on the single-CTA kernel forced to 128 x 256
+    and to 128 x 128 tiles: repeat calls identical, and close to the plain
+    launch."""
+    import torch
+    M, N, K = 384, 1536, 4096
+    A, B = inputs.make(M, N, K, "normal", True, seed=5)
+    a, b = dev(A), dev(B)
+    try:
+        for force in (KERNELS["one_cta_256"], KERNELS["one_cta_128"]):
+            gr.gemm_relu_debug_force_kernel(force)
+            assert gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K) > 0, force
+            ws = gr.streamk_workspace(M, N, K)
+            c = gr.gemm_relu_streamk(a, b, workspace=ws)
+            c2 = gr.gemm_relu_streamk(a, b, workspace=ws)
+            ref = gr.gemm_relu(a, b)
+            torch.cuda.synchronize()
+            assert gr.status() == gr.OK
+            assert torch.equal(c.view(torch.int16), c2.view(torch.int16)), force
+            torch.testing.assert_close(c.float(), ref.float(), rtol=1e-2, atol=1e-3)
+    finally:
+        gr.gemm_relu_debug_force_kernel(0)
+
+
+# ----------------------------------------------------------------- staged operands
+
+# Row pitches that TMA cannot describe: the stream-K entry point copies A
+# and/or B into aligned rows of its workspace and runs the TMA kernel, with
+# predicated stores when C's rows are unaligned too.
+STAGED_SHAPES = [
+    (1537, 1023, 777),   # the ragged workload: A and B copied, C stored predicated
+    (2305, 1031, 333),   # two waves of tiles
+    (1000, 1024, 777),   # A copied only; B and C aligned (C by TMA)
+    (1024, 1001, 1024),  # B copied only, C predicated
+    (129, 70, 300),      # one tile, edges everywhere
+    (5000, 37, 13),      # K smaller than one k block, narrow N
+]
+
+
+@pytest.mark.parametrize("M,N,K", STAGED_SHAPES)
+def test_staged_operands_full(orc, M, N, K):
+    """Every element of the staged path against the oracle, with the
+    workspace and C inside guard bands that must stay untouched."""
+    import torch
+    n = gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K)
+    assert n > 0
+    A, B = inputs.make(M, N, K, "normal", True, seed=M + N + 5 * K)
+    a, b = dev(A), dev(B)
+    pad = 4096
+    wbuf = torch.full((n + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
+    cbuf = torch.full((M * N + 2 * pad,), float("nan"), dtype=torch.float16, device="cuda")
+    c = cbuf[pad:pad + M * N].view(M, N)
+    gr.gemm_relu_streamk(a, b, out=c, workspace=wbuf[pad:pad + n])
+    torch.cuda.synchronize()
+    assert gr.status() == gr.OK
+    assert (wbuf[:pad] == 0x5A).all() and (wbuf[pad + n:] == 0x5A).all()
+    assert torch.isnan(cbuf[:pad]).all() and torch.isnan(cbuf[pad + M * N:]).all()
+    want = oracle_threaded(orc, A, B)
+    assert_parity(host(c), want, abs_dot(A, B), K, (M, N, K, "staged"))
+    # same bits on a second call (and whatever the workspace held), and the
+    # same bits as gemm_relu_f16's predicated-load kernel
+    c2 = gr.gemm_relu_streamk(a, b, workspace=wbuf[pad:pad + n].random_(0, 256))
+    plain = gr.gemm_relu(a, b)
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16), c2.view(torch.int16))
+    assert torch.equal(c.view(torch.int16), plain.view(torch.int16))
+
+
+def test_staged_misaligned_bases(orc):
+    """Aligned pitches but operands starting 2 bytes past a 16-byte boundary:
+    without room in the workspace the predicated-load kernel runs, with room
+    the operands are copied; both meet the contract against the oracle."""
+    import torch
+    M, N, K = 700, 1536, 512
+    A, B = inputs.make(M, N, K, "normal", True, seed=11)
+    abuf = torch.empty(M * K + 8, dtype=torch.float16, device="cuda")
+    bbuf = torch.empty(K * N + 8, dtype=torch.float16, device="cuda")
+    a = abuf[1:1 + M * K].view(M, K)
+    b = bbuf[3:3 + K * N].view(K, N)
+    a.copy_(torch.from_numpy(A))
+    b.copy_(torch.from_numpy(B))
+    assert gr.gemm_relu_f16_path(a.data_ptr(), b.data_ptr(), a.data_ptr(), M, N, K) == gr.PATH_LSU
+    want = oracle_threaded(orc, A, B)
+    tight = gr.streamk_workspace(M, N, K)
+    roomy = torch.empty(2 * (M * K + K * N) + 4096, dtype=torch.uint8, device="cuda")
+    outs = []
+    for ws, what in ((tight, "predicated loads"), (roomy, "copied operands")):
+        outs.append(gr.gemm_relu_streamk(a, b, workspace=ws))
+        assert gr.status() == gr.OK
+        assert_parity(host(outs[-1]), want, abs_dot(A, B), K, (M, N, K, what))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_staged_workspace_errors():
+    """Odd pitches need the workspace the query reports: a smaller or
+    misaligned one is refused with GEMMRELU_ERR_WORKSPACE."""
+    import torch
+    M, N, K = 300, 200, 99
+    n = gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K)
+    a = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    b = torch.zeros((K, N), dtype=torch.float16, device="cuda")
+    c = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    ws = torch.empty(n + 16, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = (a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K)
+    assert gr.gemm_relu_f16_streamk(*args, ws.data_ptr(), n - 1, s) == gr.ERR_WORKSPACE
+    assert gr.gemm_relu_f16_streamk(*args, None, 0, s) == gr.ERR_WORKSPACE
+    assert gr.gemm_relu_f16_streamk(*args, ws.data_ptr() + 8, n, s) == gr.ERR_WORKSPACE
+    assert gr.gemm_relu_f16_streamk(*args, ws.data_ptr(), n, s) == gr.OK
+    torch.cuda.synchronize()
+
+
 def test_streamk_falls_back_without_a_cut():
     import torch
-    # 1024 x 2048 x 512: 32 tiles, fewer than the SMs -> plain kernel, no workspace
+    # 1024 x 2048 x 512: 32 pair tiles, fewer than the SM pairs, and the
+    # pair kernel has no sub-wave schedule -> plain kernel, no workspace
     assert gr.gemm_relu_f16_streamk_workspace_bytes(1024, 2048, 512) == 0
     A, B = inputs.make(1024, 2048, 512, seed=3)
     a, b = dev(A), dev(B)

@@ -75,6 +75,8 @@ def lib():
         L.flash_attention_f16.restype = i32
         L.gemm_relu_debug_streamk.argtypes = [i32]
         L.gemm_relu_debug_streamk.restype = i32
+        L.gemm_relu_debug_streamk_pieces.argtypes = [i32]
+        L.gemm_relu_debug_streamk_pieces.restype = i32
         L.gemm_relu_debug_set_panel.argtypes = [i32]
         L.gemm_relu_debug_set_panel.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
@@ -156,11 +158,15 @@ def gemm_relu_debug_force_split(which):
     return lib().gemm_relu_debug_force_split(int(which))
 
 
-SK_NORMAL, SK_HEAD_PUBLISHES, SK_TAIL_LATE = 0, 1, 2
+SK_NORMAL, SK_HEAD_PUBLISHES, SK_TAIL_LATE, SK_HEAD_LATE = 0, 1, 2, 3
 
 
 def gemm_relu_debug_streamk(mode):
     return lib().gemm_relu_debug_streamk(int(mode))
+
+
+def gemm_relu_debug_streamk_pieces(pieces):
+    return lib().gemm_relu_debug_streamk_pieces(int(pieces))
 
 
 def gemm_relu_debug_set_panel(rows):
@@ -224,7 +230,8 @@ def streamk_workspace(M, N, K, device=None):
 
 def gemm_relu_streamk(a, b, out=None, workspace=None, stream=None):
     """Same result as gemm_relu (up to fp32 summation order in the tiles the
-    schedule cuts), with a stream-K schedule for the partial last wave."""
+    schedule cuts), with a stream-K schedule for a partial wave and operands
+    whose rows TMA cannot describe copied into aligned rows of `workspace`."""
     _check_operands(a, b)
     c = _out(a, b, out)
     M, K = a.shape

@@ -8,7 +8,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = [os.path.join(CSRC, "gemm_relu_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_relu_kernels.cuh", "gemm_relu_splitk.cuh", "gemm_relu_2sm.cuh", "gemm_relu_gemv.cuh", "flash_attention.cuh", "sm103.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_relu_kernels.cuh", "gemm_relu_splitk.cuh", "gemm_relu_2sm.cuh", "gemm_relu_gemv.cuh", "flash_attention.cuh", "sm103.cuh", "gemm_relu_stage.cuh")] + [
     os.path.join(INCLUDE, "gemm_relu.h"), os.path.join(INCLUDE, "flash_attention.h")]
 LIB = os.path.join(PKG, "libgemmrelu.so")
 

@@ -357,6 +357,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // k head of a tile cut with the next pair: add its k tail if
                 // it is there; else publish the head and finish only if the
                 // tail arrived meanwhile
+                if (p.sk_mode == 3)
+                    fused::sk_test_delay(200000);
                 int add = preloaded ? 1 : 0;
                 if (!preloaded) {
                     if (p.sk_mode == 0 &&

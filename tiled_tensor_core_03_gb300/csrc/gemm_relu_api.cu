@@ -25,6 +25,7 @@
 #include "gemm_relu_2sm.cuh"
 #include "gemm_relu_gemv.cuh"
 #include "flash_attention.cuh"
+#include "gemm_relu_stage.cuh"
 
 namespace {
 
@@ -46,6 +47,7 @@ std::atomic<int> g_force_kernel{0};   // 0 auto, 1 one CTA x 256, 2 one CTA x 12
 std::atomic<int> g_force_split{0};    // 0 auto, 1 two-stage split-K form only
 std::atomic<int> g_panel_rows{0};     // 0 the default panel, else output rows per panel
 std::atomic<int> g_sk_mode{0};        // stream-K fix-up test mode (0 normal)
+std::atomic<int> g_sk_pieces{0};      // sub-wave pieces per tile (0: the library's choice)
 // Starts from a value drawn per process, so that state words a stream-K call
 // of another process left behind in reused device memory are unlikely to
 // carry the tag of one of this process's calls.
@@ -96,7 +98,7 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
-    bool attr_fused[4] = {false, false, false, false};
+    bool attr_fused[6] = {false, false, false, false, false, false};
     bool attr_split[4] = {false, false, false, false};
     bool attr_split_cluster[4] = {false, false, false, false};
     int split_pairs[4] = {};  // max resident CTA pairs of the cluster form, per bms index
@@ -151,12 +153,13 @@ EncodeTiledFn encode_fn() {
 // Row-major fp16 matrix rows x cols (cols contiguous), box box_cols x box_rows,
 // 128-byte swizzle (or none), zero fill outside the matrix.
 bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, uint32_t box_cols,
-              uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+              uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+              int64_t pitch = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)(pitch > 0 ? pitch : cols) * 2};  // row pitch, bytes
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
@@ -297,16 +300,15 @@ int fused_bn(int64_t M, int64_t N, int sms) {
     return (double)w128 * 0.7 < (double)w256 ? 128 : 256;
 }
 
-template <bool kTma, int kBN>
+template <bool kTma, int kBN, bool kTmaStore = kTma>
 int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensorMap &mC,
                     const gemmrelu::fused::Params &p, const gemmrelu::fused::MapsFor<kTma> &rm,
-                    cudaStream_t stream, DeviceState *ds, bool &attr_done) {
+                    int64_t grid, cudaStream_t stream, bool &attr_done) {
     namespace F = gemmrelu::fused;
-    auto kern = F::gemm_relu_fused_kernel<kTma, kBN>;
+    auto kern = F::gemm_relu_fused_kernel<kTma, kBN, kTmaStore>;
     constexpr uint32_t smem = F::Tile<kBN, kTma>::kSmemBytes;
     if (!ensure_smem_attr(attr_done, kern, smem))
         return GEMMRELU_ERR_LAUNCH;
-    const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
     // (stream-K needs no co-residency: its fix-up never waits for another CTA)
     return launch_kernel(kern, (unsigned)grid, F::Roles<kTma>::kThreads, smem, stream,
                          false, 1, mA, mB, mC, p, rm);
@@ -315,6 +317,7 @@ int launch_fused_bn(const CUtensorMap &mA, const CUtensorMap &mB, const CUtensor
 // Stream-K part of a fused launch: dp_tiles < num_tiles, with its workspace.
 struct StreamK {
     int64_t dp_tiles = -1;     // -1: plain data-parallel launch
+    int64_t ctas = 0;          // grid of a stream-K launch
     float *part = nullptr;     // k-tail slots
     float *head = nullptr;     // k-head slots
     uint32_t *flags = nullptr; // fix-up state words
@@ -482,6 +485,9 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     p.sk_flags = sk.flags;
     p.epoch = sk.epoch;
     p.sk_mode = g_sk_mode.load();
+    // persistent grid: one CTA per tile up to one per SM; a stream-K launch
+    // has its plan's grid (one CTA per k range)
+    const int64_t grid = sk.dp_tiles >= 0 ? sk.ctas : std::min<int64_t>(p.num_tiles, ds->sms);
     CUtensorMap mA, mB, mC;
     std::memset(&mA, 0, sizeof(mA));
     std::memset(&mB, 0, sizeof(mB));
@@ -492,9 +498,9 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
         return GEMMRELU_ERR_LAUNCH;
     const F::NoMaps none{};
     if (bn == 256)
-        return launch_fused_bn<true, 256>(mA, mB, mC, p, none, stream, ds, ds->attr_fused[0]);
+        return launch_fused_bn<true, 256>(mA, mB, mC, p, none, grid, stream, ds->attr_fused[0]);
     if (path == 1)
-        return launch_fused_bn<true, 128>(mA, mB, mC, p, none, stream, ds, ds->attr_fused[2]);
+        return launch_fused_bn<true, 128>(mA, mB, mC, p, none, grid, stream, ds->attr_fused[2]);
     // predicated-load kernel: one tensor map per row residue modulo 8 of A and B
     F::RowMaps rm;
     std::memset(&rm, 0, sizeof(rm));
@@ -503,38 +509,179 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
             (r < K && !make_row_map(&rm.b[r], B, K, N, r, F::Tile<128, false>::BN + 8, 8)))
             return GEMMRELU_ERR_LAUNCH;
     }
-    return launch_fused_bn<false, 128>(mA, mB, mC, p, rm, stream, ds, ds->attr_fused[3]);
+    return launch_fused_bn<false, 128>(mA, mB, mC, p, rm, grid, stream, ds->attr_fused[3]);
+}
+
+// ---------------------------------------------------------------- staged operands
+// Operands whose rows TMA cannot describe, copied once into aligned rows in
+// the caller's workspace (see gemm_relu_stage.cuh): A (M x K) when its pitch
+// or base is not 16-byte aligned, B (K x N) likewise, each at a 256-byte
+// boundary with its pitch rounded up to 8 elements.
+int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct StageLayout {
+    bool a = false, b = false;       // which operands are copied
+    size_t a_bytes = 0, b_bytes = 0; // their copies, each rounded to 256 bytes
+    size_t bytes() const { return a_bytes + b_bytes; }
+};
+
+StageLayout stage_layout(bool stage_a, bool stage_b, int64_t M, int64_t N, int64_t K) {
+    StageLayout L;
+    L.a = stage_a;
+    L.b = stage_b;
+    L.a_bytes = stage_a ? round256((size_t)M * (size_t)round8(K) * 2) : 0;
+    L.b_bytes = stage_b ? round256((size_t)K * (size_t)round8(N) * 2) : 0;
+    return L;
+}
+
+// The staged GEMM: one copy kernel for the operands that need it, then the
+// single-CTA TMA kernel on the copies (and on the operands that did not),
+// storing C by TMA when its rows allow, else with predicated stores.  Both
+// launches are programmatic dependents, so the GEMM's set-up overlaps the copy.
+int launch_staged(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                  const StageLayout &L, void *workspace, cudaStream_t stream, DeviceState *ds) {
+    namespace F = gemmrelu::fused;
+    namespace G = gemmrelu::stage;
+    char *ws = static_cast<char *>(workspace);
+    const uint16_t *a = static_cast<const uint16_t *>(A), *b = static_cast<const uint16_t *>(B);
+    int64_t lda = K, ldb = N;
+    G::Params sp{};
+    int jobs = 0;
+    int64_t chunks[2] = {0, 0};
+    if (L.a) {
+        lda = round8(K);
+        sp.job[jobs] = G::Job{a, reinterpret_cast<uint16_t *>(ws), M, K, lda};
+        chunks[jobs++] = M * (lda / 8);
+        a = reinterpret_cast<const uint16_t *>(ws);
+    }
+    if (L.b) {
+        ldb = round8(N);
+        sp.job[jobs] = G::Job{b, reinterpret_cast<uint16_t *>(ws + L.a_bytes), K, N, ldb};
+        chunks[jobs++] = K * (ldb / 8);
+        b = reinterpret_cast<const uint16_t *>(ws + L.a_bytes);
+    }
+    sp.chunks0 = chunks[0];
+    sp.total = chunks[0] + chunks[1];
+    if (jobs == 1)
+        sp.job[1] = sp.job[0];   // (never read: every chunk index is below chunks0)
+    if (jobs > 0) {              // (none when only C's rows are unaligned)
+        const int64_t blocks = std::max<int64_t>(
+            1, std::min<int64_t>((sp.total + 255) / 256, (int64_t)8 * ds->sms));
+        const int rc =
+            launch_kernel(G::stage_rows_kernel, (unsigned)blocks, 256, 0, stream, false, 1, sp);
+        if (rc != GEMMRELU_OK)
+            return rc;
+    }
+
+    F::Params p{};
+    p.A = a;
+    p.B = b;
+    p.C = static_cast<uint16_t *>(C);
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.num_kb = (int)((K + F::BK - 1) / F::BK);
+    const int bn = fused_bn(M, N, ds->sms);
+    p.m_tiles = (M + F::BM - 1) / F::BM;
+    p.n_tiles = (N + bn - 1) / bn;
+    p.num_tiles = p.m_tiles * p.n_tiles;
+    p.panel = panel_tiles(F::BM, K);
+    p.drop_arrive = g_drop_arrive.load();
+    p.wait_limit_ns = wait_limit_ns();
+    p.dp_tiles = p.num_tiles;
+    p.sk_mode = g_sk_mode.load();
+    const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
+    CUtensorMap mA, mB, mC;
+    std::memset(&mC, 0, sizeof(mC));
+    const bool c_tma = tma_ok(C, N);
+    if (!make_map(&mA, a, M, K, F::BK, F::BM, CU_TENSOR_MAP_SWIZZLE_128B, lda) ||
+        !make_map(&mB, b, K, N, 64, F::BK, CU_TENSOR_MAP_SWIZZLE_128B, ldb) ||
+        (c_tma && !make_map(&mC, C, M, N, 64, 32)))
+        return GEMMRELU_ERR_LAUNCH;
+    const F::NoMaps none{};
+    if (bn == 256)
+        return c_tma ? launch_fused_bn<true, 256, true>(mA, mB, mC, p, none, grid, stream,
+                                                        ds->attr_fused[0])
+                     : launch_fused_bn<true, 256, false>(mA, mB, mC, p, none, grid, stream,
+                                                         ds->attr_fused[4]);
+    return c_tma ? launch_fused_bn<true, 128, true>(mA, mB, mC, p, none, grid, stream,
+                                                    ds->attr_fused[2])
+                 : launch_fused_bn<true, 128, false>(mA, mB, mC, p, none, grid, stream,
+                                                     ds->attr_fused[5]);
 }
 
 // ---------------------------------------------------------------- stream-K plan
-// When a shape's tiles do not fill a whole number of waves, all full waves
-// but the last run data-parallel and the rest is spread evenly over the
-// workers (CTA pairs for the pair kernel, CTAs for the single-CTA kernel).
+// TMA path only.  When a shape's tiles do not fill a whole number of waves,
+// all full waves but the last run data-parallel and the rest is spread
+// evenly over the workers (CTA pairs for the pair kernel, CTAs for the
+// single-CTA kernel).
+//
+// With fewer single-CTA tiles than SMs (a partial first wave: small output,
+// long K), each tile's k blocks are cut into `pieces` equal ranges on
+// pieces * T <= SMs CTAs, pieces = nkb / 128 + 1 clamped to [2, 8] (ranges of
+// about 64 to 128 k blocks).  This applies to the single-CTA kernel's shapes
+// with M > 64 (fewer rows go to the split-K and GEMV kernels) when the ranges
+// come out at least kSkMinSaved k blocks of a 128-column tile shorter than a
+// tile, and when an operand that several tiles share fits in half of L2.
+// Measured on GB300 (us, plain / 2 / 3 / 4 / 6 pieces): each cut adds a few
+// microseconds of fp32 piece traffic through L2 after the last MMA, worth
+// some 20 to 40 k blocks of MMA, so short ranges lose (1024^3 on 128 x 128
+// tiles 8.6 / 12.0; 200 x 3000 x 2048 12.7 / 14.2; 128 x 4096 x 4096
+// 19.3 / 17.4 / 20.4 / 24.4; 128 x 4096 x 8192 33.6 / 24.9 / 26.4 / 29.4) and
+// long ones gain (128 x 2048 x 16384 61.9 / 38.3 / 33.6 / 33.8 / 39.2;
+// 100 x 1024 x 32768 118.8 / 66.5 / 52.1 / 46.9 / 46.8).  Tiles cut at
+// different k offsets read a shared operand at different times, and a large
+// one is re-read from DRAM (192 x 6400 x 8192, a 105 MB B shared by two rows
+// of tiles: 34.9 -> 45.1 us with 100 tiles spread over 152 CTAs), which also
+// lost on an HBM-bound shape (128 x 12800 x 8192: 40.9 -> 47.6 us).
 struct SkPlan {
     bool pair = false;
     int64_t dp_tiles = -1;     // -1: no stream-K part
-    int64_t ctas = 0;          // workspace slots (one per CTA)
+    int64_t ctas = 0;          // grid, and workspace slots (one per CTA)
 };
 
-SkPlan streamk_plan(int64_t M, int64_t N, int sms) {
+constexpr int64_t kSkMinSaved = 32;
+constexpr int64_t kSkMaxSharedBytes = 64ll << 20;
+
+SkPlan streamk_plan(int64_t M, int64_t N, int64_t K, int path, int sms) {
+    namespace F = gemmrelu::fused;
     SkPlan plan;
-    int64_t T, G;
-    if (M <= V::kMaxM)
+    if (M <= V::kMaxM || path != 1)
         return plan;  // decode-like rows: the GEMV kernel (or the plain one) serves them
     if (use_pair(M, N, sms, 1)) {
+        const int64_t T = ((M + 255) / 256) * ((N + 255) / 256);
+        const int64_t G = std::min<int64_t>(T, sms / 2);
         plan.pair = true;
-        T = ((M + 255) / 256) * ((N + 255) / 256);
-        G = std::min<int64_t>(T, sms / 2);
         plan.ctas = 2 * G;
-    } else {
-        if (fused_bn(M, N, sms) != 256)
-            return plan;
-        T = ((M + 127) / 128) * ((N + 255) / 256);
-        G = std::min<int64_t>(T, sms);
-        plan.ctas = G;
+        if (T > G && T % G != 0)
+            plan.dp_tiles = (T / G - 1) * G;
+        return plan;
     }
-    if (T > G && T % G != 0)
-        plan.dp_tiles = (T / G - 1) * G;
+    const int bn = fused_bn(M, N, sms);
+    const int64_t m_tiles = (M + F::BM - 1) / F::BM, n_tiles = (N + bn - 1) / bn;
+    const int64_t T = m_tiles * n_tiles;
+    if (T >= sms) {
+        if (bn == 256 && T % sms != 0) {
+            plan.dp_tiles = (T / sms - 1) * sms;
+            plan.ctas = sms;
+        }
+        return plan;
+    }
+    const int64_t nkb = (K + F::BK - 1) / F::BK;
+    const int64_t pieces = g_sk_pieces.load() > 0
+                               ? g_sk_pieces.load()
+                               : std::min<int64_t>({std::max<int64_t>(nkb / 128 + 1, 2), 8,
+                                                    sms / std::max<int64_t>(T, 1)});
+    const int64_t G = pieces * T;
+    if (M <= 64 || pieces < 2 || G > sms)
+        return plan;
+    const int64_t shared_bytes = (m_tiles > 1 ? 2 * K * N : 0) + (n_tiles > 1 ? 2 * M * K : 0);
+    const int64_t longest = (nkb + pieces - 1) / pieces;
+    if (shared_bytes > kSkMaxSharedBytes || (nkb - longest) * (bn / 128) < kSkMinSaved)
+        return plan;
+    plan.dp_tiles = 0;
+    plan.ctas = G;
     return plan;
 }
 
@@ -838,10 +985,12 @@ int gemm_relu_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, i
 size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return 0;
+    if (K % 8 != 0 || N % 8 != 0)
+        return stage_layout(true, true, M, N, K).bytes();  // rows TMA cannot describe
     DeviceState *ds = nullptr;
     if (current_device_state(&ds) != GEMMRELU_OK)
         return 0;
-    const SkPlan plan = streamk_plan(M, N, ds->sms);
+    const SkPlan plan = streamk_plan(M, N, K, 1, ds->sms);
     return plan.dp_tiles < 0 ? 0 : streamk_bytes(plan.ctas);
 }
 
@@ -859,8 +1008,26 @@ int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int6
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0)
         return zero_fill(C, M, N, s);
-    const SkPlan plan = streamk_plan(M, N, ds->sms);
-    if (plan.dp_tiles < 0 || fused_path(A, B, C, M, N, K) != 1)
+    const int path = fused_path(A, B, C, M, N, K);
+    if (path == 2) {
+        // Copy the operands TMA cannot describe into the workspace, then the
+        // TMA kernel; without room for the copies (only possible when the
+        // pitches are aligned and a base is not), the predicated-load kernel.
+        // Odd pitches: the workspace must be what the query reports (room
+        // for both copies), whichever operands this call's pointers need.
+        const StageLayout L = stage_layout(!tma_ok(A, K), !tma_ok(B, N), M, N, K);
+        const bool odd = K % 8 != 0 || N % 8 != 0;
+        const size_t need = odd ? stage_layout(true, true, M, N, K).bytes() : L.bytes();
+        const bool room = need == 0 ||
+                          (workspace && workspace_bytes >= need && aligned(workspace, 16));
+        if (room)
+            return launch_staged(A, B, C, M, N, K, L, workspace, s, ds);
+        if (odd)
+            return GEMMRELU_ERR_WORKSPACE;
+        return launch_fused(A, B, C, M, N, K, s, ds);
+    }
+    const SkPlan plan = streamk_plan(M, N, K, path, ds->sms);
+    if (plan.dp_tiles < 0)
         return launch_fused(A, B, C, M, N, K, s, ds);
     if (!workspace || workspace_bytes < streamk_bytes(plan.ctas) || !aligned(workspace, 16))
         return GEMMRELU_ERR_WORKSPACE;
@@ -871,6 +1038,7 @@ int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int6
     sk.head = reinterpret_cast<float *>(ws + (size_t)plan.ctas * kSkSlotBytes);
     sk.flags = reinterpret_cast<uint32_t *>(ws + 2 * (size_t)plan.ctas * kSkSlotBytes);
     sk.epoch = next_epoch();
+    sk.ctas = plan.ctas;
     if (plan.pair)
         return launch_pair(A, B, C, M, N, K, s, ds, sk);
     return launch_fused(A, B, C, M, N, K, s, ds, sk);
@@ -994,9 +1162,16 @@ int gemm_relu_debug_force_split(int which) {
 }
 
 int gemm_relu_debug_streamk(int mode) {
-    if (mode < 0 || mode > 2)
+    if (mode < 0 || mode > 3)
         return GEMMRELU_ERR_INVALID_ARG;
     g_sk_mode.store(mode);
+    return GEMMRELU_OK;
+}
+
+int gemm_relu_debug_streamk_pieces(int pieces) {
+    if (pieces != 0 && (pieces < 2 || pieces > 8))
+        return GEMMRELU_ERR_INVALID_ARG;
+    g_sk_pieces.store(pieces);
     return GEMMRELU_OK;
 }
 

@@ -348,14 +348,18 @@ struct Params {
     // tile cut between CTA c (its k head: the first k blocks, at the end of
     // c's range) and CTA c + 1 (its k tail, at the start of c + 1's range) is
     // finished by whichever of the two gets there second (see sk_exchange):
-    // no CTA ever waits for another.  dp_tiles equal to num_tiles means no
-    // stream-K part.
+    // no CTA ever waits for another.  With fewer tiles than CTAs (dp_tiles
+    // 0, ranges shorter than a tile) a tile can be cut more than once; its
+    // cuts are then settled from right to left (see the epilogue), so the
+    // tile is always summed as p0 + (p1 + (p2 + ...)) over its pieces.
+    // dp_tiles equal to num_tiles means no stream-K part.
     int64_t dp_tiles;
     float *sk_part;        // [G] k-tail slots of BM x BN fp32, [BN/4][BM][4] each
     float *sk_head;        // [G] k-head slots, same layout
     uint32_t *sk_flags;    // [G][4]: the state of each cut, one word per epilogue warp
     uint32_t epoch;        // nonzero, below 2^30, distinct per call
-    int sk_mode;           // test hook: 0 normal; 1 heads always publish; 2 also delay tails
+    int sk_mode;           // test hook: 0 normal; 1 heads always publish; 2 also delay
+                           // tails; 3 heads always publish, delayed
 };
 
 // Tensor maps of the predicated-load kernel: for each residue a modulo 8, the
@@ -374,7 +378,7 @@ struct NoMaps {};
 template <bool kTma>
 using MapsFor = typename std::conditional<kTma, NoMaps, RowMaps>::type;
 
-enum ItemKind : int { kItemFull = 0, kItemPieceOut = 1, kItemPieceIn = 2 };
+enum ItemKind : int { kItemFull = 0, kItemPieceOut = 1, kItemPieceIn = 2, kItemPieceMid = 3 };
 
 // Stream-K schedule over `num_tiles` tiles of `num_kb` k blocks run by G
 // workers (CTAs, or CTA pairs): tiles [0, dp_tiles) data-parallel, worker c
@@ -395,10 +399,11 @@ __device__ __forceinline__ int64_t sk_num_items(const SkShape &g, int64_t c, int
 }
 
 // Item i of worker c: tile id, k-block range [kb0, kb1) and kind.  A piece
-// that starts inside its tile is the tile's k tail (kItemPieceOut, stored for
-// the previous worker); one that stops inside is the k head (kItemPieceIn,
-// adds the next worker's stored tail).  Each range is at least one tile long,
-// so a piece is never both.
+// that starts inside its tile is the tile's k tail (kItemPieceOut); one that
+// stops inside is its k head (kItemPieceIn); one that does both
+// (kItemPieceMid) lies strictly inside a tile, which happens only when the
+// ranges are shorter than a tile (fewer tiles than workers).  The CTA-pair
+// kernel's schedules always have ranges of at least one tile.
 __device__ __forceinline__ void sk_item_at(const SkShape &g, int64_t c, int64_t G, int64_t i,
                                            int64_t &tile, int &kb0, int &kb1, int &kind) {
     const int64_t ndp = c < g.dp_tiles ? (g.dp_tiles - 1 - c) / G + 1 : 0;
@@ -416,7 +421,8 @@ __device__ __forceinline__ void sk_item_at(const SkShape &g, int64_t c, int64_t 
     kb0 = (int)((s > lo ? s : lo) - lo);
     kb1 = (int)((e < lo + g.num_kb ? e : lo + g.num_kb) - lo);
     tile = g.dp_tiles + t;
-    kind = kb0 > 0 ? kItemPieceOut : (kb1 < g.num_kb ? kItemPieceIn : kItemFull);
+    kind = kb0 > 0 ? (kb1 < g.num_kb ? kItemPieceMid : kItemPieceOut)
+                   : (kb1 < g.num_kb ? kItemPieceIn : kItemFull);
 }
 
 __device__ __forceinline__ int64_t num_items(const Params &p, int64_t c, int64_t G) {
@@ -496,8 +502,22 @@ __device__ __forceinline__ void add_slot32(uint32_t (&r)[32], const float *slot,
     }
 }
 
-// Test hook: keep a k tail from publishing for about `ns` (bounded by the
-// global timer), so the k head's side of the exchange runs first.
+// r[j] = column col0 + j of this lane's row of a published piece.
+__device__ __forceinline__ void load_slot32(uint32_t (&r)[32], const float *slot, int row,
+                                            int col0) {
+    const float4 *s = reinterpret_cast<const float4 *>(slot) + (size_t)(col0 / 4) * 128 + row;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = __ldcg(s + (size_t)i * 128);
+        r[4 * i] = __float_as_uint(x.x);
+        r[4 * i + 1] = __float_as_uint(x.y);
+        r[4 * i + 2] = __float_as_uint(x.z);
+        r[4 * i + 3] = __float_as_uint(x.w);
+    }
+}
+
+// Test hook: keep one side of a cut from publishing for about `ns` (bounded
+// by the global timer), so the other side of the exchange runs first.
 __device__ __forceinline__ void sk_test_delay(uint64_t ns) {
     const uint64_t t0 = global_timer_ns();
     while (global_timer_ns() - t0 < ns)
@@ -565,7 +585,9 @@ struct Roles {
     static constexpr int kThreads = 32 * (kLoadWarps + 1 + kEpiWarps);
 };
 
-template <bool kTma, int kBN>
+// kTma: operands by TMA (else the predicated-load producer); kTmaStore: C by
+// TMA (else predicated stores, for a C whose rows TMA cannot describe).
+template <bool kTma, int kBN, bool kTmaStore = kTma>
 __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     gemm_relu_fused_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
@@ -614,7 +636,8 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
     if (kTma && warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
-        tma_prefetch_map(&tmC);
+        if (kTmaStore)
+            tma_prefetch_map(&tmC);
     }
     if (warp == R::kMmaWarp) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -890,25 +913,31 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
         const uint32_t stage_base = base + kOffEpi + (uint32_t)ew * T::kEpiBufs * kEpiBuf;
         uint32_t nstores = 0;
         const int64_t items = num_items(p, blockIdx.x, gridDim.x);
-        // Stream-K (TMA path only).  This CTA holds the k tail of the tile cut
-        // with the previous CTA (its first stream-K item) and the k head of
-        // the tile cut with the next one (its last item).  When the k head is
-        // last and the next CTA's k tail is already published by the time the
-        // item before the k head has been read, the tail is copied into the
-        // other TMEM buffer (not used again) while the MMA works on the head,
-        // and the head's epilogue adds the two buffers; otherwise the two
-        // sides meet through sk_exchange.
+        // Stream-K.  Cut k (0 < k < G) sits at position k * W / G of the
+        // stream-K k blocks; its state word is sk_flags[k][q], the pieces on
+        // its two sides go to sk_part[k] (everything of the tile right of the
+        // cut) and sk_head[k - 1] (CTA k - 1's own piece, left of the cut).
+        // This CTA's first stream-K item starts at cut c = blockIdx.x and its
+        // last ends at cut c + 1.  When the k head is the last item and the
+        // next CTA's k tail is already published by the time the item before
+        // it has been read, the tail is copied into the other TMEM buffer (not
+        // used again) while the MMA works on the head, and the head's epilogue
+        // adds the two buffers; otherwise the two sides meet through
+        // sk_exchange.
         int64_t last_t = 0;
         int last_kb0 = 0, last_kb1 = 0, last_kind = kItemFull;
         if (items > 0)
             item_at(p, blockIdx.x, gridDim.x, items - 1, last_t, last_kb0, last_kb1, last_kind);
+        // (not in the predicated-load kernel: its 13 warps leave 128
+        // registers a thread, which the pre-load's 128 in-flight values
+        // would overflow)
         const bool head_last = kTma && last_kind == kItemPieceIn;
         const uint32_t partner_buf = tmem_base + lane_base + (uint32_t)((items - 2) & 1) * BN;
-        uint32_t *const head_cut = p.sk_flags + (blockIdx.x + 1) * 4 + q;  // this CTA's k head
-        uint32_t *const tail_cut = p.sk_flags + blockIdx.x * 4 + q;        // this CTA's k tail
-        const float *const next_tail = p.sk_part + (size_t)(blockIdx.x + 1) * BN * BM;
-        const float *const prev_head =
-            blockIdx.x > 0 ? p.sk_head + (size_t)(blockIdx.x - 1) * BN * BM : nullptr;
+        const int64_t sk_w = (p.num_tiles - p.dp_tiles) * (int64_t)p.num_kb;
+        constexpr size_t kSlot = (size_t)BN * BM;
+        auto cut_state = [&](int64_t k) { return p.sk_flags + k * 4 + q; };
+        uint32_t *const head_cut = cut_state((int64_t)blockIdx.x + 1);   // this CTA's k head
+        const float *const next_tail = p.sk_part + (size_t)(blockIdx.x + 1) * kSlot;
         bool preloaded = false;
         auto try_preload = [&]() {
             if (p.sk_mode != 0 || sk_peek(head_cut, lane) != sk_tail_tag(p.epoch))
@@ -919,9 +948,24 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 *head_cut = 0u;  // consumed
             preloaded = true;
         };
-        // Stores tile t from accumulator `acc` (+ the TMEM partner buffer
-        // when add == 1, + a published piece when add == 2) as ReLU'd fp16.
-        auto store_tile = [&](int64_t t, uint32_t acc, int add, const float *piece) {
+        // A sum of pieces in fp32: the TMEM accumulator `acc` (or the
+        // published piece `from`, when set) plus either the TMEM partner
+        // buffer (when `partner`) or the published piece `add` (when set).
+        // sum32: columns col0 .. col0 + 31 of this lane's row.
+        auto sum32 = [&](uint32_t acc, const float *from, bool partner, const float *add,
+                         int col0, uint32_t (&r)[32]) {
+            if (from)
+                load_slot32(r, from, row_in_tile, col0);
+            else
+                tmem_ld_x32_sync(acc + (uint32_t)col0, r);
+            if (partner)
+                add_tmem(r, partner_buf + (uint32_t)col0);
+            else if (add)
+                add_slot32(r, add, row_in_tile, col0);
+        };
+        // Stores tile t from a sum of pieces (as in sum32) as ReLU'd fp16.
+        auto store_tile = [&](int64_t t, uint32_t acc, const float *from, bool partner,
+                              const float *add) {
             int64_t mb, nb;
             tile_coord(t, p.m_tiles, p.n_tiles, p.panel, mb, nb);
             const int64_t row0 = mb * BM + 32 * q;
@@ -932,25 +976,15 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 if (row0 >= p.M || col0 >= p.N)
                     continue;  // warp-uniform: nothing of this chunk is in C
                 uint32_t r[32], h[32];
-                const uint32_t taddr = acc + 64 * c;
-                tmem_ld_x32_sync(taddr, r);
-                if (kTma && add == 1)
-                    add_tmem(r, partner_buf + 64 * c);
-                if (kTma && add == 2)
-                    add_slot32(r, piece, row_in_tile, 64 * c);
+                sum32(acc, from, partner, add, 64 * c, r);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
-                tmem_ld_x32_sync(taddr + 32, r);
-                if (kTma && add == 1)
-                    add_tmem(r, partner_buf + 64 * c + 32);
-                if (kTma && add == 2)
-                    add_slot32(r, piece, row_in_tile, 64 * c + 32);
+                sum32(acc, from, partner, add, 64 * c + 32, r);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
-
-                if constexpr (kTma) {
+                if constexpr (kTmaStore) {
                     const uint32_t sb = stage_base + (nstores & 1u) * kEpiBuf;
                     // the store issued two chunks ago from this buffer must
                     // have finished reading it
@@ -998,12 +1032,12 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 }
             }
         };
-        // Publishes this lane's row of accumulator `acc` into `slot`.
-        auto publish = [&](float *slot, uint32_t acc) {
+        // Publishes this lane's row of a sum of pieces (as in sum32) into `slot`.
+        auto publish = [&](float *slot, uint32_t acc, const float *from, const float *add) {
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_x32_sync(acc + 32 * c, r);
+                sum32(acc, from, false, add, 32 * c, r);
                 piece_store32(slot, row_in_tile, 32 * c, r);
             }
         };
@@ -1022,46 +1056,60 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                 break;
             tc_fence_after_sync();
             const uint32_t acc = tmem_base + lane_base + buf * BN;
-            if (kTma && kind == kItemPieceOut) {
-                // k tail of a tile cut with the previous CTA: publish it; if
-                // that CTA's k head was published first, finish the tile here.
-                if (p.sk_mode == 2)
+            // the sum this warp holds of the tile: acc (or `from`) + partner + add
+            const float *from = nullptr, *add = nullptr;
+            bool partner = false;
+            bool holds = true;  // this warp still holds part of the tile's sum
+            if (kind == kItemPieceIn || kind == kItemPieceMid) {
+                // The cut at the piece's end first (this CTA is its left side):
+                // add the next CTA's published right part if it is there; else
+                // publish the piece, and go on only if the right part arrived
+                // meanwhile (otherwise its owner goes on with this piece).
+                if (p.sk_mode == 3)
                     sk_test_delay(200000);
-                publish(p.sk_part + (size_t)blockIdx.x * BN * BM, acc);
-                if (sk_exchange(tail_cut, sk_tail_tag(p.epoch), lane) == sk_head_tag(p.epoch)) {
-                    store_tile(t, acc, 2, prev_head);
+                if (preloaded) {
+                    partner = true;
+                } else if (p.sk_mode == 0 && sk_peek(head_cut, lane) == sk_tail_tag(p.epoch)) {
+                    add = next_tail;
+                } else {
+                    publish(p.sk_head + (size_t)blockIdx.x * kSlot, acc, nullptr, nullptr);
+                    if (sk_exchange(head_cut, sk_head_tag(p.epoch), lane) == sk_tail_tag(p.epoch))
+                        add = next_tail;
+                    else
+                        holds = false;
+                }
+                if (add) {
                     __syncwarp();
                     if (lane == 0)
-                        *tail_cut = 0u;  // consumed
+                        *head_cut = 0u;  // consumed (nobody touches it again in this call)
                 }
-            } else if (kTma && kind == kItemPieceIn) {
-                // k head of a tile cut with the next CTA: add its k tail if it
-                // is there; else publish the head, and finish only if the tail
-                // arrived meanwhile.
-                int add = preloaded ? 1 : 0;
-                if (!preloaded) {
-                    if (p.sk_mode == 0 && sk_peek(head_cut, lane) == sk_tail_tag(p.epoch)) {
-                        add = 2;
-                    } else {
-                        publish(p.sk_head + (size_t)blockIdx.x * BN * BM, acc);
-                        if (sk_exchange(head_cut, sk_head_tag(p.epoch), lane) ==
-                            sk_tail_tag(p.epoch))
-                            add = 2;
-                        else
-                            add = -1;  // the next CTA finishes the tile
-                    }
-                }
-                if (add >= 0) {
-                    store_tile(t, acc, add, next_tail);
-                    if (add == 2) {
-                        __syncwarp();
-                        if (lane == 0)
-                            *head_cut = 0u;  // consumed
-                    }
-                }
-            } else {
-                store_tile(t, acc, 0, nullptr);
             }
+            // Then the cuts to the left, while the sum held starts inside the
+            // tile: publish it as the right part of cut k; if cut k's left
+            // piece (CTA k - 1's) was published first, add it, and the sum now
+            // starts where CTA k - 1's range does.
+            int64_t k = blockIdx.x;
+            bool inside = kb0 > 0;
+            if (holds && inside && p.sk_mode == 2)
+                sk_test_delay(200000);
+            const int64_t tile_lo = (t - p.dp_tiles) * (int64_t)p.num_kb;
+            while (holds && inside) {
+                float *const slot = p.sk_part + (size_t)k * kSlot;
+                publish(slot, acc, from, add);
+                if (sk_exchange(cut_state(k), sk_tail_tag(p.epoch), lane) != sk_head_tag(p.epoch)) {
+                    holds = false;  // CTA k - 1 finishes the cut
+                    break;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    *cut_state(k) = 0u;  // consumed
+                from = slot;
+                add = p.sk_head + (size_t)(k - 1) * kSlot;
+                inside = (k - 1) * sk_w / (int64_t)gridDim.x > tile_lo;
+                --k;
+            }
+            if (holds)
+                store_tile(t, acc, from, partner, add);
             // accumulator buffer fully read: hand it back to the MMA warp
             tc_fence_before_sync();
             __syncwarp();
@@ -1070,7 +1118,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             if (head_last && items >= 2 && i == items - 2)
                 try_preload();
         }
-        if constexpr (kTma) {
+        if constexpr (kTmaStore) {
             if (lane == 0)
                 bulk_wait_group<0>();
         }
