@@ -78,25 +78,27 @@ def kernel_source_hash():
 #   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
 #       --clock-control none -k regex:"gemm_relu_pair|splitk" -s 6 -c 6 --csv
 #       python bench.py --steps 3 --warmup 3 --no-cpu-baseline --no-extra
-# and the same with -k regex:gemm_relu (gemv, flash) -s 3 (6) -c 3 and
-# --workload square256 / square1024 / ragged (decode1; attn, attn_causal),
-# each run after the same command had exited 0 without ncu, on the sources
-# whose kernel_source_hash() is `source_hash`.  Launches inside the CUDA
-# graphs of the small workloads leave C in L2 (write 0 in the launch).  When
-# the sources differ, the figures no longer describe the kernels that run and
-# the bench reports null with the reason.
+# and the same with -k regex:gemm_relu (gemv, flash; "gemm_relu|stage_rows")
+# -s 3 (6) -c 3 (6) and --workload square256 / square1024 (decode1; attn,
+# attn_causal; ragged), each run after the same command had exited 0 without
+# ncu, on the sources whose kernel_source_hash() is `source_hash`.  Launches
+# inside the CUDA graphs of the small workloads leave C in L2 (write 0 in the
+# launch).  The ragged workload's figure is its GEMM launch; the copy kernel
+# before it moves another 3,991,211 bytes (A and B read once).  When the
+# sources differ, the figures no longer describe the kernels that run and the
+# bench reports null with the reason.
 TRAFFIC_CAPTURE = {
-    "source_hash": "eff1b09e15aca6c7",
+    "source_hash": "841c48406a39245d",
     # mean of three captured launches each (read + write)
     "bytes": {
-        ('streamk', 4096, 4096, 4096): 112_143_104,
-        ('splitk', 16, 8192, 8192): 134_632_363,
-        ('fused', 256, 256, 256): 328_021,
-        ('fused', 1024, 1024, 1024): 4_260_523,
-        ('fused', 1537, 1023, 777): 4_032_256,
-        ('fused', 1, 8192, 8192): 135_437_141,
-        ('attn', 4, 4096, 32, 128, False): 514_276_267,
-        ('attn', 4, 4096, 32, 128, True): 516_430_592,
+        ('streamk', 4096, 4096, 4096): 109_308_757,
+        ('splitk', 16, 8192, 8192): 134_633_387,
+        ('fused', 256, 256, 256): 327_936,
+        ('fused', 1024, 1024, 1024): 4_260_352,
+        ('fused', 1537, 1023, 777): 4_055_723,
+        ('fused', 1, 8192, 8192): 135_321_856,
+        ('attn', 4, 4096, 32, 128, False): 513_093_888,
+        ('attn', 4, 4096, 32, 128, True): 516_279_808,
     },
 }
 
@@ -1008,7 +1010,7 @@ def measure_config(gpu, w, steps, warmup, world, cpu_budget, want_cpu=True):
     out = {
         "workload": describe(w),
         "kernel": f"gemm_relu_f16_streamk {w.M}x{w.N}x{w.K}: {kern}, as the library selects",
-        "path": {1: "tma", 2: "predicated"}.get(path, str(path)),
+        "path": {1: "tma", 2: "staged (rows not 16-byte aligned)"}.get(path, str(path)),
         "ms": ms, "tflops": w.flops / (ms * 1e-3) / 1e12, "gbs": w.bytes / (ms * 1e-3) / 1e9,
         "roofline": gpu.roofline(f"gemm_relu_f16_streamk {w.M}x{w.N}x{w.K} ({kern})", w.flops,
                                  w.bytes, ms, ("fused", w.M, w.N, w.K)),
