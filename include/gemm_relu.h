@@ -60,7 +60,7 @@ typedef enum {
  * One fused kernel, chosen per shape:
  *   - M >= 256 and N >= 256 with TMA-capable A, B, C: 256 x 256 tiles on CTA
  *     pairs (tcgen05.mma.cta_group::2), when that needs no more waves than
- *     one CTA per 128 x 256 tile;
+ *     one CTA per 128 x 256 tile and the 128 x 128 tiles outnumber the SMs;
  *   - M <= 2, or M <= 4 unless the case below applies with one CTA pair
  *     per 128 columns all resident at once (2 * ceil(N / 128) <= SMs), with
  *     TMA-capable A and B: the GEMV kernel -- B streamed through shared
@@ -252,6 +252,26 @@ const char *gemm_relu_strerror(int code);
  */
 int gemm_relu_f16_path(const void *A, const void *B, const void *C,
                        int64_t M, int64_t N, int64_t K);
+
+/* The kernels gemm_relu_f16 chooses from (see gemm_relu_f16_kernel). */
+typedef enum {
+    GEMMRELU_KERNEL_PAIR = 1,        /* 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2) */
+    GEMMRELU_KERNEL_ONE_CTA_256 = 2, /* 128 x 256 tiles, one CTA each */
+    GEMMRELU_KERNEL_ONE_CTA_128 = 3, /* 128 x 128 tiles, one CTA each */
+    GEMMRELU_KERNEL_PREDICATED = 4,  /* predicated loads and stores, 128 x 128 tiles */
+    GEMMRELU_KERNEL_GEMV = 5,        /* CUDA-core GEMV for decode-like rows */
+    GEMMRELU_KERNEL_SPLITK_PAIR = 6  /* split-K CTA-pair form with split_k = 2 */
+} gemmrelu_kernel;
+
+/*
+ * gemm_relu_f16_kernel -- which kernel gemm_relu_f16 would launch for these
+ * arguments on the current device (the choice depends on its SM count and on
+ * the gemm_relu_debug_force_* hooks): a gemmrelu_kernel code, 0 = nothing to
+ * launch (empty output or K == 0), -1 = invalid arguments, -2 = no usable
+ * CUDA device.  Launches nothing.
+ */
+int gemm_relu_f16_kernel(const void *A, const void *B, const void *C,
+                         int64_t M, int64_t N, int64_t K);
 
 /*
  * gemm_relu_tile_coord -- the tile rasteriser, evaluated on the host (the

@@ -51,6 +51,32 @@ def test_ragged_takes_lsu_path_and_aligned_takes_tma():
     assert gr.gemm_relu_f16_path(a.data_ptr(), a.data_ptr(), a.data_ptr(), 1024, 1024, 1024) == gr.PATH_TMA
 
 
+def test_kernel_choice_per_shape():
+    """gemm_relu_f16_kernel reports the routing: decode rows to the GEMV
+    kernel, skinny rows to the split-K pair form, outputs that one wave of
+    128 x 128 tiles covers to the single-CTA kernel, larger ones to CTA
+    pairs, unaligned rows to the predicated-load kernel; the force hooks
+    override it."""
+    import torch
+    buf = torch.empty(64 << 20, dtype=torch.float16, device="cuda")
+    p = buf.data_ptr()
+    cases = [((1, 8192, 8192), gr.KERNEL_GEMV), ((16, 8192, 8192), gr.KERNEL_SPLITK_PAIR),
+             ((256, 256, 256), gr.KERNEL_ONE_CTA_128), ((1024, 1024, 1024), gr.KERNEL_ONE_CTA_128),
+             ((1920, 1280, 1024), gr.KERNEL_ONE_CTA_128), ((2048, 2048, 2048), gr.KERNEL_PAIR),
+             ((4096, 4096, 4096), gr.KERNEL_PAIR), ((128, 4096, 4096), gr.KERNEL_ONE_CTA_128),
+             ((1537, 1023, 777), gr.KERNEL_PREDICATED)]
+    for (M, N, K), want in cases:
+        assert gr.gemm_relu_f16_kernel(p, p, p, M, N, K) == want, (M, N, K)
+    assert gr.gemm_relu_f16_kernel(p, p, p, 64, 64, 0) == 0
+    assert gr.gemm_relu_f16_kernel(p, p, p, -1, 64, 64) == -1
+    try:
+        for force, want in ((1, gr.KERNEL_ONE_CTA_256), (2, gr.KERNEL_ONE_CTA_128), (3, gr.KERNEL_PAIR)):
+            gr.gemm_relu_debug_force_kernel(force)
+            assert gr.gemm_relu_f16_kernel(p, p, p, 1024, 1024, 1024) == want, force
+    finally:
+        gr.gemm_relu_debug_force_kernel(0)
+
+
 @pytest.fixture(scope="module")
 def square4096(orc):
     """The 4096^3 workload, its full oracle output (rows over the host's
@@ -644,9 +670,9 @@ GEMV_CASES = [(1, 8, 8), (1, 8192, 8192), (2, 264, 72), (3, 520, 1000), (4, 136,
 
 @pytest.fixture
 def forced_gemv():
-    gr.gemm_relu_debug_force_kernel(gr.KERNEL_GEMV)
+    gr.gemm_relu_debug_force_kernel(gr.FORCE_GEMV)
     yield
-    gr.gemm_relu_debug_force_kernel(gr.KERNEL_AUTO)
+    gr.gemm_relu_debug_force_kernel(gr.FORCE_AUTO)
 
 
 @pytest.mark.parametrize("M,N,K", GEMV_CASES)
@@ -688,12 +714,12 @@ def test_decode_rows_routing(orc):
         a, b = dev(A), dev(B)
         auto = gr.gemm_relu(a, b)
         try:
-            gr.gemm_relu_debug_force_kernel(gr.KERNEL_GEMV)
+            gr.gemm_relu_debug_force_kernel(gr.FORCE_GEMV)
             gemv = gr.gemm_relu(a, b)
-            gr.gemm_relu_debug_force_kernel(gr.KERNEL_ONE_CTA_256)
+            gr.gemm_relu_debug_force_kernel(gr.FORCE_ONE_CTA_256)
             tile = gr.gemm_relu(a, b)
         finally:
-            gr.gemm_relu_debug_force_kernel(gr.KERNEL_AUTO)
+            gr.gemm_relu_debug_force_kernel(gr.FORCE_AUTO)
         split2 = gr.gemm_relu_splitk(a, b, 2)
         assert gr.status() == gr.OK
         same = gemv if route == "gemv" else split2

@@ -74,7 +74,7 @@ def test_pair_kernel_dropped_arrival_times_out_and_recovers(orc):
     M, N, K = 512, 1024, 512
     A, B = inputs.make(M, N, K, seed=10)
     a, b = dev(A), dev(B)
-    gr.gemm_relu_debug_force_kernel(gr.KERNEL_PAIR)
+    gr.gemm_relu_debug_force_kernel(gr.FORCE_PAIR)
     try:
         gr.gemm_relu_debug_set(1, 20_000_000)
         gr.gemm_relu(a, b)

@@ -26,6 +26,14 @@ ERR_SCRATCH_LIMIT = 7
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 PATH_NONE, PATH_TMA, PATH_LSU = 0, 1, 2
+(KERNEL_PAIR, KERNEL_ONE_CTA_256, KERNEL_ONE_CTA_128, KERNEL_PREDICATED, KERNEL_GEMV,
+ KERNEL_SPLITK_PAIR) = 1, 2, 3, 4, 5, 6
+KERNEL_NAMES = {KERNEL_PAIR: "CTA-pair kernel (256 x 256 tiles)",
+                KERNEL_ONE_CTA_256: "single-CTA kernel (128 x 256 tiles)",
+                KERNEL_ONE_CTA_128: "single-CTA kernel (128 x 128 tiles)",
+                KERNEL_PREDICATED: "predicated-load kernel (128 x 128 tiles)",
+                KERNEL_GEMV: "GEMV kernel",
+                KERNEL_SPLITK_PAIR: "split-K CTA-pair form (split 2)"}
 
 _lib = None
 
@@ -64,6 +72,8 @@ def lib():
         L.gemm_relu_strerror.restype = ctypes.c_char_p
         L.gemm_relu_f16_path.argtypes = [vp, vp, vp, i64, i64, i64]
         L.gemm_relu_f16_path.restype = i32
+        L.gemm_relu_f16_kernel.argtypes = [vp, vp, vp, i64, i64, i64]
+        L.gemm_relu_f16_kernel.restype = i32
         L.gemm_relu_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
                                            ctypes.POINTER(i64)]
         L.gemm_relu_tile_coord.restype = i32
@@ -135,6 +145,10 @@ def gemm_relu_f16_path(A, B, C, M, N, K):
     return lib().gemm_relu_f16_path(A, B, C, M, N, K)
 
 
+def gemm_relu_f16_kernel(A, B, C, M, N, K):
+    return lib().gemm_relu_f16_kernel(A, B, C, M, N, K)
+
+
 def gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel):
     mb, nb = ctypes.c_int64(), ctypes.c_int64()
     rc = lib().gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel, ctypes.byref(mb),
@@ -144,7 +158,8 @@ def gemm_relu_tile_coord(tile, m_tiles, n_tiles, panel):
     return mb.value, nb.value
 
 
-KERNEL_AUTO, KERNEL_ONE_CTA_256, KERNEL_ONE_CTA_128, KERNEL_PAIR, KERNEL_GEMV = 0, 1, 2, 3, 4
+# codes of gemm_relu_debug_force_kernel (not the gemm_relu_f16_kernel codes above)
+FORCE_AUTO, FORCE_ONE_CTA_256, FORCE_ONE_CTA_128, FORCE_PAIR, FORCE_GEMV = 0, 1, 2, 3, 4
 
 
 def gemm_relu_debug_force_kernel(which):

@@ -436,8 +436,14 @@ int launch_gemv(const void *A, const void *B, void *C, int64_t M, int64_t N, int
 }
 
 // Whether gemm_relu_f16 runs the CTA-pair kernel: TMA operands, at least one
-// full 256 x 256 tile, and no more weighted waves than the single-CTA choice
-// (a 256 x 256 pair tile does the work of two 128 x 256 tiles on two SMs).
+// full 256 x 256 tile, more 128 x 128 tiles than SMs, and no more weighted
+// waves than the single-CTA choice (a 256 x 256 pair tile does the work of
+// two 128 x 256 tiles on two SMs).  When one wave of 128 x 128 single-CTA
+// tiles covers the output, it spreads the work over up to four times as
+// many SMs as the pair tiles: measured faster wherever it fits (GB300, us,
+// pair -> 128 x 128: 1024^3 9.75 -> 8.65, 1024 x 1024 x 4096 22.4 -> 19.6,
+// 1536^3 12.1 -> 11.1, 1920 x 1280 x 1024 10.4 -> 9.2), while at 2048^3, two
+// waves of them, the pair stays ahead (15.9 against 20.5).
 bool use_pair(int64_t M, int64_t N, int sms, int path) {
     const int force = g_force_kernel.load();
     if (force == 3)
@@ -446,6 +452,8 @@ bool use_pair(int64_t M, int64_t N, int sms, int path) {
         return false;
     if (path != 1 || M < 256 || N < 256 || sms < 2)
         return false;
+    if (((M + 127) / 128) * ((N + 127) / 128) <= sms)
+        return false;
     const int64_t pair_waves = ((M + 255) / 256 * ((N + 255) / 256) + sms / 2 - 1) / (sms / 2);
     const int64_t one_waves = ((M + 127) / 128 * ((N + 255) / 256) + sms - 1) / sms;
     return pair_waves <= one_waves;
@@ -453,16 +461,41 @@ bool use_pair(int64_t M, int64_t N, int sms, int path) {
 
 int launch_skinny_split(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                         cudaStream_t stream, DeviceState *ds);
+// The kernel gemm_relu_f16 runs for these arguments (a GEMMRELU_KERNEL_*
+// code; 0: nothing to launch, -1: invalid arguments).  launch_fused routes by
+// this same function.
+int kernel_for(const void *A, const void *B, const void *C, int64_t M, int64_t N, int64_t K,
+               int sms) {
+    const int path = fused_path(A, B, C, M, N, K);
+    if (path <= 0)
+        return path;
+    if (use_gemv(A, B, M, N, K, sms))
+        return GEMMRELU_KERNEL_GEMV;
+    if (use_skinny_split(A, B, M, N, K, sms))
+        return GEMMRELU_KERNEL_SPLITK_PAIR;
+    if (use_pair(M, N, sms, path))
+        return GEMMRELU_KERNEL_PAIR;
+    if (path == 2)
+        return GEMMRELU_KERNEL_PREDICATED;
+    return fused_bn(M, N, sms) == 256 ? GEMMRELU_KERNEL_ONE_CTA_256 : GEMMRELU_KERNEL_ONE_CTA_128;
+}
+
 int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                  cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
     namespace F = gemmrelu::fused;
     const int path = fused_path(A, B, C, M, N, K);
-    if (sk.dp_tiles < 0 && use_gemv(A, B, M, N, K, ds->sms))
-        return launch_gemv(A, B, C, M, N, K, stream, ds);
-    if (sk.dp_tiles < 0 && use_skinny_split(A, B, M, N, K, ds->sms))
-        return launch_skinny_split(A, B, C, M, N, K, stream, ds);
-    if (sk.dp_tiles < 0 && use_pair(M, N, ds->sms, path))
-        return launch_pair(A, B, C, M, N, K, stream, ds);
+    if (sk.dp_tiles < 0) {
+        switch (kernel_for(A, B, C, M, N, K, ds->sms)) {
+        case GEMMRELU_KERNEL_GEMV:
+            return launch_gemv(A, B, C, M, N, K, stream, ds);
+        case GEMMRELU_KERNEL_SPLITK_PAIR:
+            return launch_skinny_split(A, B, C, M, N, K, stream, ds);
+        case GEMMRELU_KERNEL_PAIR:
+            return launch_pair(A, B, C, M, N, K, stream, ds);
+        default:
+            break;  // one of the single-CTA kernels, below
+        }
+    }
     F::Params p{};
     p.A = static_cast<const uint16_t *>(A);
     p.B = static_cast<const uint16_t *>(B);
@@ -1133,6 +1166,17 @@ const char *gemm_relu_strerror(int code) {
 int gemm_relu_f16_path(const void *A, const void *B, const void *C, int64_t M, int64_t N,
                        int64_t K) {
     return fused_path(A, B, C, M, N, K);
+}
+
+int gemm_relu_f16_kernel(const void *A, const void *B, const void *C, int64_t M, int64_t N,
+                         int64_t K) {
+    const int path = fused_path(A, B, C, M, N, K);
+    if (path <= 0)
+        return path;
+    DeviceState *ds = nullptr;
+    if (current_device_state(&ds) != GEMMRELU_OK)
+        return -2;
+    return kernel_for(A, B, C, M, N, K, ds->sms);
 }
 
 int gemm_relu_tile_coord(int64_t tile, int64_t m_tiles, int64_t n_tiles, int panel, int64_t *m_blk,
