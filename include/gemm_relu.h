@@ -85,10 +85,10 @@ int gemm_relu_f16(const void *A, const void *B, void *C,
 /*
  * gemm_relu_f16_streamk_workspace_bytes -- bytes of device workspace that
  * gemm_relu_f16_streamk needs for these sizes on the current device (its SM
- * count decides the schedule): when K or N is not a multiple of 8, room for
- * aligned copies of A and B; otherwise the stream-K schedule's, 0 when the
- * call would run no stream-K part.  0 for invalid arguments, or when no CUDA
- * device is available.
+ * count decides the schedule): the stream-K schedule's slots (none when the
+ * call would run no stream-K part) and, when K or N is not a multiple of 8,
+ * room for aligned copies of A and B before them.  0 for invalid arguments,
+ * or when no CUDA device is available.
  */
 size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -119,9 +119,12 @@ size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * Operands: when A's or B's rows do not start on 16-byte boundaries (a row
  * pitch that is not a multiple of 8 elements, or an unaligned base), the
  * call first copies that operand into rows of pitch round_up(cols, 8) in
- * the workspace (one extra kernel), then runs the TMA kernel on the copy;
- * when C's rows are unaligned, the kernel stores C with predicated stores.
- * The result has the same bits as gemm_relu_f16's predicated-load kernel.
+ * the workspace (one extra kernel), then runs on the copies the kernel the
+ * TMA path would choose for these sizes (CTA pairs or single CTAs, with the
+ * stream-K schedule above when it applies); when C's rows are unaligned, that
+ * kernel stores C with predicated stores.  Where the copies run on the
+ * single-CTA kernel with no tile cut, the result has the same bits as
+ * gemm_relu_f16's predicated-load kernel.
  *
  * workspace: device buffer of at least
  *            gemm_relu_f16_streamk_workspace_bytes(M, N, K) bytes, 16-byte

@@ -69,6 +69,7 @@ constexpr uint32_t kIdesc = make_idesc_f16_f32(BMP, BNP, 0, 1);
 constexpr int kThreads = 192;                   // producer, MMA, 4 epilogue warps
 
 struct Params {
+    uint16_t *C;                                // for predicated stores (kTmaStore false)
     int M, N, K;
     int num_kb;
     int64_t m_tiles, n_tiles, num_tiles;        // 256 x 256 tiles
@@ -89,6 +90,9 @@ struct Params {
     int sk_mode;           // test hook, as in the single-CTA kernel
 };
 
+// kTmaStore: C by TMA stores (else predicated stores, for a C whose rows TMA
+// cannot describe; A and B always come by TMA).
+template <bool kTmaStore = true>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_relu_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
@@ -132,7 +136,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
-        tma_prefetch_map(&tmC);
+        if (kTmaStore)
+            tma_prefetch_map(&tmC);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
@@ -312,21 +317,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     h[16 + j] = relu_pack_half2(r[2 * j], r[2 * j + 1]);
-                const uint32_t sb = stage_base + (nstores & 1u) * kEpiBuf;
-                if (lane == 0)
-                    bulk_wait_group_read<1>();
-                __syncwarp();
+                if constexpr (kTmaStore) {
+                    const uint32_t sb = stage_base + (nstores & 1u) * kEpiBuf;
+                    if (lane == 0)
+                        bulk_wait_group_read<1>();
+                    __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(sb + sw128_offset(lane, j), h[4 * j], h[4 * j + 1], h[4 * j + 2],
-                                 h[4 * j + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmC, sb, (int32_t)col0, (int32_t)row0);
-                    bulk_commit_group();
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(sb + sw128_offset(lane, j), h[4 * j], h[4 * j + 1],
+                                     h[4 * j + 2], h[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, sb, (int32_t)col0, (int32_t)row0);
+                        bulk_commit_group();
+                    }
+                    ++nstores;
+                } else {
+                    store_rows_predicated(stage_base, h, p.C, p.M, p.N, row0, col0, lane);
                 }
-                ++nstores;
             }
         };
         for (int64_t i = 0; i < items; ++i) {
@@ -390,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (head_last && items >= 2 && i == items - 2)
                 try_preload();
         }
-        if (lane == 0)
+        if (kTmaStore && lane == 0)
             bulk_wait_group<0>();
     }
 

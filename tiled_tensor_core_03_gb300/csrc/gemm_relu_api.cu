@@ -103,6 +103,7 @@ struct DeviceState {
     bool attr_split_cluster[4] = {false, false, false, false};
     int split_pairs[4] = {};  // max resident CTA pairs of the cluster form, per bms index
     bool attr_pair = false;
+    bool attr_pair_pred = false;
     bool attr_gemv[4] = {false, false, false, false};
     bool attr_attn[2] = {false, false};
 };
@@ -325,12 +326,16 @@ struct StreamK {
 };
 
 // ---------------------------------------------------------------- CTA-pair launch
-// 256 x 256 tiles on CTA pairs (2-SM MMA).  TMA path only.
+// 256 x 256 tiles on CTA pairs (2-SM MMA).  A and B by TMA (row pitches lda,
+// ldb elements: K and N for the caller's own operands, wider for staged
+// copies); C by TMA stores when its rows allow, else predicated stores.
 int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
+                cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK(),
+                int64_t lda = 0, int64_t ldb = 0) {
     namespace P = gemmrelu::pair;
     namespace F = gemmrelu::fused;
     P::Params p{};
+    p.C = static_cast<uint16_t *>(C);
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;
@@ -347,15 +352,24 @@ int launch_pair(const void *A, const void *B, void *C, int64_t M, int64_t N, int
     p.sk_flags = sk.flags;
     p.epoch = sk.epoch;
     p.sk_mode = g_sk_mode.load();
+    const bool c_tma = tma_ok(C, N);
     CUtensorMap mA, mB, mC;
-    if (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
-        !make_map(&mC, C, M, N, 64, 32))
-        return GEMMRELU_ERR_LAUNCH;
-    if (!ensure_smem_attr(ds->attr_pair, P::gemm_relu_pair_kernel, P::kSmemBytes))
+    std::memset(&mC, 0, sizeof(mC));
+    if (!make_map(&mA, A, M, K, F::BK, F::BM, CU_TENSOR_MAP_SWIZZLE_128B, lda) ||
+        !make_map(&mB, B, K, N, 64, F::BK, CU_TENSOR_MAP_SWIZZLE_128B, ldb) ||
+        (c_tma && !make_map(&mC, C, M, N, 64, 32)))
         return GEMMRELU_ERR_LAUNCH;
     const int64_t pairs = std::min<int64_t>(p.num_tiles, ds->sms / 2);
-    // stream-K: pairs wait on flags of their neighbours -> cooperative launch
-    return launch_kernel(P::gemm_relu_pair_kernel, (unsigned)(2 * pairs), P::kThreads,
+    // (stream-K needs no co-residency: its fix-up never waits for another CTA)
+    if (c_tma) {
+        if (!ensure_smem_attr(ds->attr_pair, P::gemm_relu_pair_kernel<true>, P::kSmemBytes))
+            return GEMMRELU_ERR_LAUNCH;
+        return launch_kernel(P::gemm_relu_pair_kernel<true>, (unsigned)(2 * pairs), P::kThreads,
+                             P::kSmemBytes, stream, false, 1, mA, mB, mC, p);
+    }
+    if (!ensure_smem_attr(ds->attr_pair_pred, P::gemm_relu_pair_kernel<false>, P::kSmemBytes))
+        return GEMMRELU_ERR_LAUNCH;
+    return launch_kernel(P::gemm_relu_pair_kernel<false>, (unsigned)(2 * pairs), P::kThreads,
                          P::kSmemBytes, stream, false, 1, mA, mB, mC, p);
 }
 
@@ -480,22 +494,13 @@ int kernel_for(const void *A, const void *B, const void *C, int64_t M, int64_t N
     return fused_bn(M, N, sms) == 256 ? GEMMRELU_KERNEL_ONE_CTA_256 : GEMMRELU_KERNEL_ONE_CTA_128;
 }
 
-int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                 cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
+// The single-CTA kernel.  tma_loads: A and B by TMA with row pitches lda,
+// ldb (elements), C by TMA stores when its rows allow, else predicated
+// stores; otherwise the predicated-load kernel (pitches K and N).
+int launch_single_cta(const void *A, int64_t lda, const void *B, int64_t ldb, void *C, int64_t M,
+                      int64_t N, int64_t K, bool tma_loads, cudaStream_t stream, DeviceState *ds,
+                      const StreamK &sk) {
     namespace F = gemmrelu::fused;
-    const int path = fused_path(A, B, C, M, N, K);
-    if (sk.dp_tiles < 0) {
-        switch (kernel_for(A, B, C, M, N, K, ds->sms)) {
-        case GEMMRELU_KERNEL_GEMV:
-            return launch_gemv(A, B, C, M, N, K, stream, ds);
-        case GEMMRELU_KERNEL_SPLITK_PAIR:
-            return launch_skinny_split(A, B, C, M, N, K, stream, ds);
-        case GEMMRELU_KERNEL_PAIR:
-            return launch_pair(A, B, C, M, N, K, stream, ds);
-        default:
-            break;  // one of the single-CTA kernels, below
-        }
-    }
     F::Params p{};
     p.A = static_cast<const uint16_t *>(A);
     p.B = static_cast<const uint16_t *>(B);
@@ -505,7 +510,7 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     p.K = (int)K;
     p.num_kb = (int)((K + F::BK - 1) / F::BK);
     // The predicated-load producer is laid out for 128 x 128 tiles.
-    const int bn = path == 1 ? fused_bn(M, N, ds->sms) : 128;
+    const int bn = tma_loads ? fused_bn(M, N, ds->sms) : 128;
     p.m_tiles = (M + F::BM - 1) / F::BM;
     p.n_tiles = (N + bn - 1) / bn;
     p.num_tiles = p.m_tiles * p.n_tiles;
@@ -525,15 +530,23 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     std::memset(&mA, 0, sizeof(mA));
     std::memset(&mB, 0, sizeof(mB));
     std::memset(&mC, 0, sizeof(mC));
-    if (path == 1 &&
-        (!make_map(&mA, A, M, K, F::BK, F::BM) || !make_map(&mB, B, K, N, 64, F::BK) ||
-         !make_map(&mC, C, M, N, 64, 32)))
-        return GEMMRELU_ERR_LAUNCH;
-    const F::NoMaps none{};
-    if (bn == 256)
-        return launch_fused_bn<true, 256>(mA, mB, mC, p, none, grid, stream, ds->attr_fused[0]);
-    if (path == 1)
-        return launch_fused_bn<true, 128>(mA, mB, mC, p, none, grid, stream, ds->attr_fused[2]);
+    if (tma_loads) {
+        const bool c_tma = tma_ok(C, N);
+        if (!make_map(&mA, A, M, K, F::BK, F::BM, CU_TENSOR_MAP_SWIZZLE_128B, lda) ||
+            !make_map(&mB, B, K, N, 64, F::BK, CU_TENSOR_MAP_SWIZZLE_128B, ldb) ||
+            (c_tma && !make_map(&mC, C, M, N, 64, 32)))
+            return GEMMRELU_ERR_LAUNCH;
+        const F::NoMaps none{};
+        if (bn == 256)
+            return c_tma ? launch_fused_bn<true, 256, true>(mA, mB, mC, p, none, grid, stream,
+                                                            ds->attr_fused[0])
+                         : launch_fused_bn<true, 256, false>(mA, mB, mC, p, none, grid, stream,
+                                                             ds->attr_fused[4]);
+        return c_tma ? launch_fused_bn<true, 128, true>(mA, mB, mC, p, none, grid, stream,
+                                                        ds->attr_fused[2])
+                     : launch_fused_bn<true, 128, false>(mA, mB, mC, p, none, grid, stream,
+                                                         ds->attr_fused[5]);
+    }
     // predicated-load kernel: one tensor map per row residue modulo 8 of A and B
     F::RowMaps rm;
     std::memset(&rm, 0, sizeof(rm));
@@ -545,103 +558,22 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
     return launch_fused_bn<false, 128>(mA, mB, mC, p, rm, grid, stream, ds->attr_fused[3]);
 }
 
-// ---------------------------------------------------------------- staged operands
-// Operands whose rows TMA cannot describe, copied once into aligned rows in
-// the caller's workspace (see gemm_relu_stage.cuh): A (M x K) when its pitch
-// or base is not 16-byte aligned, B (K x N) likewise, each at a 256-byte
-// boundary with its pitch rounded up to 8 elements.
-int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
-size_t round256(size_t x) { return (x + 255) / 256 * 256; }
-
-struct StageLayout {
-    bool a = false, b = false;       // which operands are copied
-    size_t a_bytes = 0, b_bytes = 0; // their copies, each rounded to 256 bytes
-    size_t bytes() const { return a_bytes + b_bytes; }
-};
-
-StageLayout stage_layout(bool stage_a, bool stage_b, int64_t M, int64_t N, int64_t K) {
-    StageLayout L;
-    L.a = stage_a;
-    L.b = stage_b;
-    L.a_bytes = stage_a ? round256((size_t)M * (size_t)round8(K) * 2) : 0;
-    L.b_bytes = stage_b ? round256((size_t)K * (size_t)round8(N) * 2) : 0;
-    return L;
-}
-
-// The staged GEMM: one copy kernel for the operands that need it, then the
-// single-CTA TMA kernel on the copies (and on the operands that did not),
-// storing C by TMA when its rows allow, else with predicated stores.  Both
-// launches are programmatic dependents, so the GEMM's set-up overlaps the copy.
-int launch_staged(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                  const StageLayout &L, void *workspace, cudaStream_t stream, DeviceState *ds) {
-    namespace F = gemmrelu::fused;
-    namespace G = gemmrelu::stage;
-    char *ws = static_cast<char *>(workspace);
-    const uint16_t *a = static_cast<const uint16_t *>(A), *b = static_cast<const uint16_t *>(B);
-    int64_t lda = K, ldb = N;
-    G::Params sp{};
-    int jobs = 0;
-    int64_t chunks[2] = {0, 0};
-    if (L.a) {
-        lda = round8(K);
-        sp.job[jobs] = G::Job{a, reinterpret_cast<uint16_t *>(ws), M, K, lda};
-        chunks[jobs++] = M * (lda / 8);
-        a = reinterpret_cast<const uint16_t *>(ws);
+int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                 cudaStream_t stream, DeviceState *ds, const StreamK &sk = StreamK()) {
+    const int path = fused_path(A, B, C, M, N, K);
+    if (sk.dp_tiles < 0) {
+        switch (kernel_for(A, B, C, M, N, K, ds->sms)) {
+        case GEMMRELU_KERNEL_GEMV:
+            return launch_gemv(A, B, C, M, N, K, stream, ds);
+        case GEMMRELU_KERNEL_SPLITK_PAIR:
+            return launch_skinny_split(A, B, C, M, N, K, stream, ds);
+        case GEMMRELU_KERNEL_PAIR:
+            return launch_pair(A, B, C, M, N, K, stream, ds);
+        default:
+            break;  // one of the single-CTA kernels, below
+        }
     }
-    if (L.b) {
-        ldb = round8(N);
-        sp.job[jobs] = G::Job{b, reinterpret_cast<uint16_t *>(ws + L.a_bytes), K, N, ldb};
-        chunks[jobs++] = K * (ldb / 8);
-        b = reinterpret_cast<const uint16_t *>(ws + L.a_bytes);
-    }
-    sp.chunks0 = chunks[0];
-    sp.total = chunks[0] + chunks[1];
-    if (jobs == 1)
-        sp.job[1] = sp.job[0];   // (never read: every chunk index is below chunks0)
-    if (jobs > 0) {              // (none when only C's rows are unaligned)
-        const int64_t blocks = std::max<int64_t>(
-            1, std::min<int64_t>((sp.total + 255) / 256, (int64_t)8 * ds->sms));
-        const int rc =
-            launch_kernel(G::stage_rows_kernel, (unsigned)blocks, 256, 0, stream, false, 1, sp);
-        if (rc != GEMMRELU_OK)
-            return rc;
-    }
-
-    F::Params p{};
-    p.A = a;
-    p.B = b;
-    p.C = static_cast<uint16_t *>(C);
-    p.M = (int)M;
-    p.N = (int)N;
-    p.K = (int)K;
-    p.num_kb = (int)((K + F::BK - 1) / F::BK);
-    const int bn = fused_bn(M, N, ds->sms);
-    p.m_tiles = (M + F::BM - 1) / F::BM;
-    p.n_tiles = (N + bn - 1) / bn;
-    p.num_tiles = p.m_tiles * p.n_tiles;
-    p.panel = panel_tiles(F::BM, K);
-    p.drop_arrive = g_drop_arrive.load();
-    p.wait_limit_ns = wait_limit_ns();
-    p.dp_tiles = p.num_tiles;
-    p.sk_mode = g_sk_mode.load();
-    const int64_t grid = std::min<int64_t>(p.num_tiles, ds->sms);
-    CUtensorMap mA, mB, mC;
-    std::memset(&mC, 0, sizeof(mC));
-    const bool c_tma = tma_ok(C, N);
-    if (!make_map(&mA, a, M, K, F::BK, F::BM, CU_TENSOR_MAP_SWIZZLE_128B, lda) ||
-        !make_map(&mB, b, K, N, 64, F::BK, CU_TENSOR_MAP_SWIZZLE_128B, ldb) ||
-        (c_tma && !make_map(&mC, C, M, N, 64, 32)))
-        return GEMMRELU_ERR_LAUNCH;
-    const F::NoMaps none{};
-    if (bn == 256)
-        return c_tma ? launch_fused_bn<true, 256, true>(mA, mB, mC, p, none, grid, stream,
-                                                        ds->attr_fused[0])
-                     : launch_fused_bn<true, 256, false>(mA, mB, mC, p, none, grid, stream,
-                                                         ds->attr_fused[4]);
-    return c_tma ? launch_fused_bn<true, 128, true>(mA, mB, mC, p, none, grid, stream,
-                                                    ds->attr_fused[2])
-                 : launch_fused_bn<true, 128, false>(mA, mB, mC, p, none, grid, stream,
-                                                     ds->attr_fused[5]);
+    return launch_single_cta(A, K, B, N, C, M, N, K, path == 1, stream, ds, sk);
 }
 
 // ---------------------------------------------------------------- stream-K plan
@@ -722,6 +654,94 @@ SkPlan streamk_plan(int64_t M, int64_t N, int64_t K, int path, int sms) {
 constexpr size_t kSkSlotBytes = (size_t)256 * 128 * 4;
 size_t streamk_bytes(int64_t ctas) {
     return 2 * (size_t)ctas * kSkSlotBytes + (size_t)ctas * 4 * 4;
+}
+
+// ---------------------------------------------------------------- staged operands
+// Operands whose rows TMA cannot describe, copied once into aligned rows in
+// the caller's workspace (see gemm_relu_stage.cuh): A (M x K) when its pitch
+// or base is not 16-byte aligned, B (K x N) likewise, each at a 256-byte
+// boundary with its pitch rounded up to 8 elements.  The stream-K slots, when
+// the GEMM on the copies has a stream-K part, follow the copies.
+int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct StageLayout {
+    bool a = false, b = false;       // which operands are copied
+    size_t a_bytes = 0, b_bytes = 0; // their copies, each rounded to 256 bytes
+    size_t bytes() const { return a_bytes + b_bytes; }
+};
+
+StageLayout stage_layout(bool stage_a, bool stage_b, int64_t M, int64_t N, int64_t K) {
+    StageLayout L;
+    L.a = stage_a;
+    L.b = stage_b;
+    L.a_bytes = stage_a ? round256((size_t)M * (size_t)round8(K) * 2) : 0;
+    L.b_bytes = stage_b ? round256((size_t)K * (size_t)round8(N) * 2) : 0;
+    return L;
+}
+
+// Workspace bytes of the stream-K part of a GEMM of these sizes on the TMA
+// path (0: none).
+size_t tma_streamk_bytes(int64_t M, int64_t N, int64_t K, int sms) {
+    const SkPlan plan = streamk_plan(M, N, K, 1, sms);
+    return plan.dp_tiles < 0 ? 0 : streamk_bytes(plan.ctas);
+}
+
+// The staged GEMM: one copy kernel for the operands that need it, then the
+// kernel the TMA path would run on aligned operands of these sizes -- the
+// CTA pair or the single-CTA kernel, with the stream-K schedule when the
+// workspace also has room for its slots -- storing C by TMA when its rows
+// allow, else with predicated stores.  The GEMM is a programmatic dependent
+// of the copy, so its set-up overlaps the copy.
+int launch_staged(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                  const StageLayout &L, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream, DeviceState *ds) {
+    namespace G = gemmrelu::stage;
+    char *ws = static_cast<char *>(workspace);
+    const uint16_t *a = static_cast<const uint16_t *>(A), *b = static_cast<const uint16_t *>(B);
+    int64_t lda = K, ldb = N;
+    G::Params sp{};
+    int jobs = 0;
+    int64_t chunks[2] = {0, 0};
+    if (L.a) {
+        lda = round8(K);
+        sp.job[jobs] = G::Job{a, reinterpret_cast<uint16_t *>(ws), M, K, lda};
+        chunks[jobs++] = M * (lda / 8);
+        a = reinterpret_cast<const uint16_t *>(ws);
+    }
+    if (L.b) {
+        ldb = round8(N);
+        sp.job[jobs] = G::Job{b, reinterpret_cast<uint16_t *>(ws + L.a_bytes), K, N, ldb};
+        chunks[jobs++] = K * (ldb / 8);
+        b = reinterpret_cast<const uint16_t *>(ws + L.a_bytes);
+    }
+    sp.chunks0 = chunks[0];
+    sp.total = chunks[0] + chunks[1];
+    if (jobs == 1)
+        sp.job[1] = sp.job[0];   // (never read: every chunk index is below chunks0)
+    if (jobs > 0) {              // (none when only C's rows are unaligned)
+        const int64_t blocks = std::max<int64_t>(
+            1, std::min<int64_t>((sp.total + 255) / 256, (int64_t)8 * ds->sms));
+        const int rc =
+            launch_kernel(G::stage_rows_kernel, (unsigned)blocks, 256, 0, stream, false, 1, sp);
+        if (rc != GEMMRELU_OK)
+            return rc;
+    }
+    const SkPlan plan = streamk_plan(M, N, K, 1, ds->sms);
+    StreamK sk;
+    if (plan.dp_tiles >= 0 && workspace_bytes >= L.bytes() + streamk_bytes(plan.ctas)) {
+        char *skw = ws + L.bytes();
+        sk.dp_tiles = plan.dp_tiles;
+        sk.ctas = plan.ctas;
+        sk.part = reinterpret_cast<float *>(skw);
+        sk.head = reinterpret_cast<float *>(skw + (size_t)plan.ctas * kSkSlotBytes);
+        sk.flags = reinterpret_cast<uint32_t *>(skw + 2 * (size_t)plan.ctas * kSkSlotBytes);
+        sk.epoch = next_epoch();
+    }
+    // (streamk_plan chose between the two kernels by the same use_pair)
+    if (use_pair(M, N, ds->sms, 1))
+        return launch_pair(a, b, C, M, N, K, stream, ds, sk, lda, ldb);
+    return launch_single_cta(a, lda, b, ldb, C, M, N, K, true, stream, ds, sk);
 }
 
 // ---------------------------------------------------------------- split-K
@@ -1018,13 +1038,12 @@ int gemm_relu_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, i
 size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return 0;
-    if (K % 8 != 0 || N % 8 != 0)
-        return stage_layout(true, true, M, N, K).bytes();  // rows TMA cannot describe
     DeviceState *ds = nullptr;
     if (current_device_state(&ds) != GEMMRELU_OK)
         return 0;
-    const SkPlan plan = streamk_plan(M, N, K, 1, ds->sms);
-    return plan.dp_tiles < 0 ? 0 : streamk_bytes(plan.ctas);
+    // rows TMA cannot describe: room for both copies before the stream-K slots
+    const size_t copies = (K % 8 != 0 || N % 8 != 0) ? stage_layout(true, true, M, N, K).bytes() : 0;
+    return copies + tma_streamk_bytes(M, N, K, ds->sms);
 }
 
 int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -1047,14 +1066,18 @@ int gemm_relu_f16_streamk(const void *A, const void *B, void *C, int64_t M, int6
         // TMA kernel; without room for the copies (only possible when the
         // pitches are aligned and a base is not), the predicated-load kernel.
         // Odd pitches: the workspace must be what the query reports (room
-        // for both copies), whichever operands this call's pointers need.
+        // for both copies and the stream-K slots), whichever operands this
+        // call's pointers need.
         const StageLayout L = stage_layout(!tma_ok(A, K), !tma_ok(B, N), M, N, K);
         const bool odd = K % 8 != 0 || N % 8 != 0;
-        const size_t need = odd ? stage_layout(true, true, M, N, K).bytes() : L.bytes();
+        const size_t need = odd ? stage_layout(true, true, M, N, K).bytes() +
+                                      tma_streamk_bytes(M, N, K, ds->sms)
+                                : L.bytes();
         const bool room = need == 0 ||
                           (workspace && workspace_bytes >= need && aligned(workspace, 16));
         if (room)
-            return launch_staged(A, B, C, M, N, K, L, workspace, s, ds);
+            return launch_staged(A, B, C, M, N, K, L, workspace, workspace ? workspace_bytes : 0, s,
+                                 ds);
         if (odd)
             return GEMMRELU_ERR_WORKSPACE;
         return launch_fused(A, B, C, M, N, K, s, ds);

@@ -242,6 +242,39 @@ __device__ __forceinline__ uint4 window16(const uint4 &v0, const uint4 &v1, cons
                       __funnelshift_r(x2, x3, f.sh), __funnelshift_r(x3, x4, f.sh));
 }
 
+// Predicated store of a warp's 32 rows x 64 fp16 columns of C (rows row0 ..,
+// columns col0 ..; this lane's row packed in h, columns in pairs) for a C
+// whose rows TMA cannot describe: the rows go through the warp's staging
+// buffer `sb` (32 x 128 bytes, 128B-swizzled) and are written row by row,
+// lane l owning columns 2l and 2l + 1, skipping rows >= M and columns >= N.
+__device__ __forceinline__ void store_rows_predicated(uint32_t sb, const uint32_t (&h)[32],
+                                                      uint16_t *C, int64_t M, int64_t N,
+                                                      int64_t row0, int64_t col0, int lane) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        st_shared_v4(sb + sw128_offset(lane, j), h[4 * j], h[4 * j + 1], h[4 * j + 2],
+                     h[4 * j + 3]);
+    __syncwarp();
+    const int64_t col = col0 + 2 * lane;
+    for (int rr = 0; rr < 32; ++rr) {
+        const int64_t row = row0 + rr;
+        if (row >= M)
+            break;
+        const uint32_t w = ld_shared_b32(sb + rr * 128u + ((((uint32_t)lane >> 2) ^ (rr & 7u)) << 4) +
+                                         ((uint32_t)lane & 3u) * 4u);
+        uint16_t *dst = C + row * N + col;
+        if (col + 1 < N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+            *reinterpret_cast<uint32_t *>(dst) = w;
+        } else {
+            if (col < N)
+                dst[0] = (uint16_t)(w & 0xffffu);
+            if (col + 1 < N)
+                dst[1] = (uint16_t)(w >> 16);
+        }
+    }
+    __syncwarp();
+}
+
 // Keep the first `nvalid` fp16 values of an 8-value chunk, zero the rest.
 __device__ __forceinline__ uint32_t keep_pair(uint32_t w, int nvalid, int e) {
     return e >= nvalid ? 0u : (e + 1 >= nvalid ? (w & 0xffffu) : w);
@@ -1003,32 +1036,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
                     }
                     ++nstores;
                 } else {
-                    const uint32_t sb = stage_base;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        st_shared_v4(sb + sw128_offset(lane, j), h[4 * j], h[4 * j + 1],
-                                     h[4 * j + 2], h[4 * j + 3]);
-                    __syncwarp();
-                    // warp writes row by row: lane l owns columns 2l, 2l+1
-                    const int64_t col = col0 + 2 * lane;
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int64_t row = row0 + rr;
-                        if (row >= p.M)
-                            break;
-                        const uint32_t w = ld_shared_b32(sb + rr * 128u +
-                                                         ((((uint32_t)lane >> 2) ^ (rr & 7u)) << 4) +
-                                                         ((uint32_t)lane & 3u) * 4u);
-                        uint16_t *dst = p.C + row * p.N + col;
-                        if (col + 1 < p.N && (reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
-                            *reinterpret_cast<uint32_t *>(dst) = w;
-                        } else {
-                            if (col < p.N)
-                                dst[0] = (uint16_t)(w & 0xffffu);
-                            if (col + 1 < p.N)
-                                dst[1] = (uint16_t)(w >> 16);
-                        }
-                    }
-                    __syncwarp();
+                    store_rows_predicated(stage_base, h, p.C, p.M, p.N, row0, col0, lane);
                 }
             }
         };
