@@ -334,7 +334,11 @@ def _sampled_parity(orc, A, B, got, what, seed=7):
     assert_parity(got[I, J], orc.gemm_relu_f16_at(A, B, I, J), abs_dot(A, B, I, J), K, (what, "samples"))
 
 
-STREAMK_SHAPES = [(4096, 4096, 4096), (2048, 5120, 320), (2000, 4104, 776), (3000, 4352, 64)]
+# Shapes whose tiles leave a thin partial last wave with a long K, so that
+# both the CTA-pair and the single-CTA kernel (128 x 256 tiles) take a
+# multi-wave stream-K schedule; 2300 x 2300 x 4000 has partial edge tiles and
+# a partial last k block.
+STREAMK_SHAPES = [(4096, 4096, 4096), (2304, 2304, 4096), (2300, 2300, 4000), (2560, 2560, 4096)]
 
 
 @pytest.fixture(params=["one_cta_256", "cta_pair"])
@@ -400,7 +404,8 @@ def test_streamk_concurrent_streams(sk_kernel):
     worker ever waits for another, so every launch completes with the same
     bits as when it runs alone."""
     import torch
-    M, N, K = 2048, 5120, 320
+    M, N, K = 2304, 2304, 4096
+    assert gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K) > 0
     A, B = inputs.make(M, N, K, "normal", True, seed=99)
     a, b = dev(A), dev(B)
     alone = gr.gemm_relu_streamk(a, b, workspace=gr.streamk_workspace(M, N, K))

@@ -51,11 +51,12 @@ def test_dropped_arrival_times_out_and_recovers(orc, kind):
 
 @pytest.mark.parametrize("kernel", [1, 3])
 def test_streamk_dropped_arrival_times_out_and_recovers(orc, kernel):
-    M, N, K = 2048, 5120, 320
+    M, N, K = 2304, 2304, 4096
     A, B = inputs.make(M, N, K, seed=9)
     a, b = dev(A), dev(B)
     gr.gemm_relu_debug_force_kernel(kernel)
     try:
+        assert gr.gemm_relu_f16_streamk_workspace_bytes(M, N, K) > 0
         ws = gr.streamk_workspace(M, N, K)
         gr.gemm_relu_debug_set(1, 20_000_000)
         gr.gemm_relu_streamk(a, b, workspace=ws)

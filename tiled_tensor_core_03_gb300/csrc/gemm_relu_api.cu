@@ -580,7 +580,15 @@ int launch_fused(const void *A, const void *B, void *C, int64_t M, int64_t N, in
 // TMA path only.  When a shape's tiles do not fill a whole number of waves,
 // all full waves but the last run data-parallel and the rest is spread
 // evenly over the workers (CTA pairs for the pair kernel, CTAs for the
-// single-CTA kernel).
+// single-CTA kernel).  The fix-up of the cut tiles (fp32 pieces through L2,
+// published after their last MMA) costs a roughly fixed 12-14 us a launch on
+// GB300, so this applies only when the plain schedule's partial last wave
+// idles longer than that: (ceil(W) - W) * k blocks >= 40 for W = tiles /
+// workers.  Measured (CTA pairs, CUDA-graph replay, us, plain / stream-K):
+// 2304^2 x 4096 (W 1.07) 41.4 / 35.8, 2560^2 x 4096 (W 1.32) 42.4 / 39.5,
+// 4096^3 (W 3.37) 82.0 / 81.7; and where the rule declines: 2304^2 x 1024
+// 15.9 / 21.5, 3072^3 (W 1.9) 35.1 / 41.8, 4096^2 x 2048 44.7 / 47.1,
+// 4608^2 x 2048 54.4 / 56.5.
 //
 // With fewer single-CTA tiles than SMs (a partial first wave: small output,
 // long K), each tile's k blocks are cut into `pieces` equal ranges on
@@ -609,17 +617,29 @@ struct SkPlan {
 constexpr int64_t kSkMinSaved = 32;
 constexpr int64_t kSkMaxSharedBytes = 64ll << 20;
 
+// Multi-wave schedules: worth it when the partial last wave leaves idle at
+// least this many k blocks' worth of each worker's time (the fraction of a
+// wave left idle, times the k blocks of a tile).
+constexpr int64_t kSkMinIdleKb = 40;
+
+bool multiwave_worth_it(int64_t T, int64_t G, int64_t nkb) {
+    if (T <= G || T % G == 0)
+        return false;
+    return (G - T % G) * nkb >= kSkMinIdleKb * G;   // (ceil(T / G) - T / G) * nkb >= 40
+}
+
 SkPlan streamk_plan(int64_t M, int64_t N, int64_t K, int path, int sms) {
     namespace F = gemmrelu::fused;
     SkPlan plan;
     if (M <= V::kMaxM || path != 1)
         return plan;  // decode-like rows: the GEMV kernel (or the plain one) serves them
+    const int64_t nkb = (K + F::BK - 1) / F::BK;
     if (use_pair(M, N, sms, 1)) {
         const int64_t T = ((M + 255) / 256) * ((N + 255) / 256);
         const int64_t G = std::min<int64_t>(T, sms / 2);
         plan.pair = true;
         plan.ctas = 2 * G;
-        if (T > G && T % G != 0)
+        if (multiwave_worth_it(T, G, nkb))
             plan.dp_tiles = (T / G - 1) * G;
         return plan;
     }
@@ -627,13 +647,12 @@ SkPlan streamk_plan(int64_t M, int64_t N, int64_t K, int path, int sms) {
     const int64_t m_tiles = (M + F::BM - 1) / F::BM, n_tiles = (N + bn - 1) / bn;
     const int64_t T = m_tiles * n_tiles;
     if (T >= sms) {
-        if (bn == 256 && T % sms != 0) {
+        if (bn == 256 && multiwave_worth_it(T, sms, nkb)) {
             plan.dp_tiles = (T / sms - 1) * sms;
             plan.ctas = sms;
         }
         return plan;
     }
-    const int64_t nkb = (K + F::BK - 1) / F::BK;
     const int64_t pieces = g_sk_pieces.load() > 0
                                ? g_sk_pieces.load()
                                : std::min<int64_t>({std::max<int64_t>(nkb / 128 + 1, 2), 8,
