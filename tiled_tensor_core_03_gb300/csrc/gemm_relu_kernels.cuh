@@ -1068,7 +1068,9 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             const float *from = nullptr, *add = nullptr;
             bool partner = false;
             bool holds = true;  // this warp still holds part of the tile's sum
-            if (kind == kItemPieceIn || kind == kItemPieceMid) {
+            // (stream-K schedules run on the TMA kernels only: the host plans
+            // none for the predicated-load kernel, whose items are all whole)
+            if (kTma && (kind == kItemPieceIn || kind == kItemPieceMid)) {
                 // The cut at the piece's end first (this CTA is its left side):
                 // add the next CTA's published right part if it is there; else
                 // publish the piece, and go on only if the right part arrived
@@ -1097,7 +1099,7 @@ __global__ void __launch_bounds__(Roles<kTma>::kThreads, 1)
             // piece (CTA k - 1's) was published first, add it, and the sum now
             // starts where CTA k - 1's range does.
             int64_t k = blockIdx.x;
-            bool inside = kb0 > 0;
+            bool inside = kTma && kb0 > 0;
             if (holds && inside && p.sk_mode == 2)
                 sk_test_delay(200000);
             const int64_t tile_lo = (t - p.dp_tiles) * (int64_t)p.num_kb;
