@@ -355,6 +355,20 @@ int gemm_relu_debug_streamk(int mode);
  */
 int gemm_relu_debug_streamk_pieces(int pieces);
 
+/*
+ * gemm_relu_debug_streamk_plan -- the stream-K schedule gemm_relu_f16_streamk
+ * would use for these sizes on operands of path `path` (1 = TMA-capable rows,
+ * 2 = rows TMA cannot describe; the staged path plans its copies as path 1)
+ * on a GPU of `sms` SMs: *dp_tiles = the data-parallel tiles before the
+ * stream-K part, or -1 for no stream-K part; *ctas = the grid of the
+ * stream-K launch (0 when none); *pair = 1 for the CTA-pair kernel.  Honours
+ * the gemm_relu_debug_force_kernel and gemm_relu_debug_streamk_pieces hooks.
+ * Host-only; never touches the device.  Returns GEMMRELU_OK, or
+ * GEMMRELU_ERR_INVALID_ARG for invalid sizes, path, sms < 2 or null outputs.
+ */
+int gemm_relu_debug_streamk_plan(int64_t M, int64_t N, int64_t K, int path, int sms,
+                                 int64_t *dp_tiles, int64_t *ctas, int *pair);
+
 #ifdef __cplusplus
 }
 #endif

@@ -139,3 +139,46 @@ def test_splitk_workspace_size(lib):
     assert gr.gemm_relu_debug_force_split(2) == gr.ERR_INVALID_ARG
     assert gr.gemm_relu_f16_splitk_workspace_bytes(0, 8, 8, 2) == 0
     assert gr.gemm_relu_f16_splitk_workspace_bytes(8, 8, 8, 0) == 0
+
+
+def test_streamk_plan_rules(lib):
+    """The stream-K schedule chosen per shape on a 152-SM GPU (host-only):
+    multi-wave schedules only where the idle part of the last wave,
+    (ceil(W) - W) x k blocks, reaches 40; sub-wave schedules for M > 64 with
+    pieces = k blocks / 128 + 1 (at least 2) per tile, pieces x tiles <= SMs,
+    at least 32 k blocks saved and a shared operand under 64 MB; nothing on
+    rows TMA cannot describe (those are staged and planned as TMA rows)."""
+    plan = gr.streamk_plan
+    # CTA pairs, multi-wave: 4096^3 (W = 3.37 on 76 pairs) keeps it; 2304^2
+    # and 2560^2 at K = 4096 (W = 1.07, 1.32) too; short K or a nearly full
+    # last wave declines
+    assert plan(4096, 4096, 4096, 152) == (152, 152, True)
+    assert plan(2304, 2304, 4096, 152) == (0, 152, True)
+    assert plan(2560, 2560, 4096, 152) == (0, 152, True)
+    for shape in [(3072, 3072, 3072), (2304, 2304, 1024), (4096, 4096, 2048), (4608, 4608, 2048)]:
+        assert plan(*shape, 152)[0] == -1, shape
+    # single CTAs, sub-wave: 2 / 3 / 5 pieces a tile on pieces x tiles CTAs
+    assert plan(200, 3000, 4096, 152) == (0, 96, False)
+    assert plan(128, 2048, 16384, 152) == (0, 48, False)
+    assert plan(100, 1024, 32768, 152) == (0, 40, False)
+    # declined: too few k blocks saved; a 105 MB B shared by two rows of
+    # tiles; more than 152 CTAs; skinny rows (split-K / GEMV); unaligned rows
+    for shape in [(1024, 1024, 1024), (192, 6400, 8192), (128, 12800, 8192), (16, 8192, 8192)]:
+        assert plan(*shape, 152)[0] == -1, shape
+    assert plan(1537, 1023, 777, 152, path=gr.PATH_LSU)[0] == -1
+    assert plan(200, 3000, 4096, 152, path=gr.PATH_LSU)[0] == -1
+    # the SM count decides: half the SMs leave no room for two pieces of 96 tiles
+    assert plan(200, 3000, 4096, 76)[0] == -1
+    try:
+        assert gr.gemm_relu_debug_streamk_pieces(4) == gr.OK
+        assert plan(128, 4096, 8192, 152) == (0, 128, False)
+        assert gr.gemm_relu_debug_force_kernel(gr.FORCE_ONE_CTA_256) == gr.OK
+        assert plan(2304, 2304, 4096, 152) == (0, 152, False)    # 162 tiles of 128 x 256
+    finally:
+        gr.gemm_relu_debug_streamk_pieces(0)
+        gr.gemm_relu_debug_force_kernel(gr.FORCE_AUTO)
+    for bad in [(0, 64, 64, 152), (64, 64, 64, 1)]:
+        with pytest.raises(ValueError):
+            plan(*bad)
+    with pytest.raises(ValueError):
+        plan(64, 64, 64, 152, path=3)

@@ -87,6 +87,9 @@ def lib():
         L.gemm_relu_debug_streamk.restype = i32
         L.gemm_relu_debug_streamk_pieces.argtypes = [i32]
         L.gemm_relu_debug_streamk_pieces.restype = i32
+        L.gemm_relu_debug_streamk_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(i64),
+                                                   ctypes.POINTER(i64), ctypes.POINTER(i32)]
+        L.gemm_relu_debug_streamk_plan.restype = i32
         L.gemm_relu_debug_set_panel.argtypes = [i32]
         L.gemm_relu_debug_set_panel.restype = i32
         L.gemm_relu_debug_set.argtypes = [i32, i64]
@@ -182,6 +185,17 @@ def gemm_relu_debug_streamk(mode):
 
 def gemm_relu_debug_streamk_pieces(pieces):
     return lib().gemm_relu_debug_streamk_pieces(int(pieces))
+
+
+def streamk_plan(M, N, K, sms, path=PATH_TMA):
+    """(dp_tiles, ctas, pair) of gemm_relu_f16_streamk's schedule on a GPU of
+    `sms` SMs; dp_tiles -1: no stream-K part.  Host-only."""
+    dp, ctas, pair = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    rc = lib().gemm_relu_debug_streamk_plan(M, N, K, path, sms, ctypes.byref(dp),
+                                            ctypes.byref(ctas), ctypes.byref(pair))
+    if rc != OK:
+        raise ValueError(strerror(rc))
+    return dp.value, ctas.value, bool(pair.value)
 
 
 def gemm_relu_debug_set_panel(rows):

@@ -1254,6 +1254,18 @@ int gemm_relu_debug_streamk(int mode) {
     return GEMMRELU_OK;
 }
 
+int gemm_relu_debug_streamk_plan(int64_t M, int64_t N, int64_t K, int path, int sms,
+                                 int64_t *dp_tiles, int64_t *ctas, int *pair) {
+    if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || sms < 2 ||
+        (path != 1 && path != 2) || !dp_tiles || !ctas || !pair)
+        return GEMMRELU_ERR_INVALID_ARG;
+    const SkPlan plan = streamk_plan(M, N, K, path, sms);
+    *dp_tiles = plan.dp_tiles;
+    *ctas = plan.dp_tiles < 0 ? 0 : plan.ctas;
+    *pair = plan.pair ? 1 : 0;
+    return GEMMRELU_OK;
+}
+
 int gemm_relu_debug_streamk_pieces(int pieces) {
     if (pieces != 0 && (pieces < 2 || pieces > 8))
         return GEMMRELU_ERR_INVALID_ARG;
