@@ -101,12 +101,15 @@ size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * the number of output tiles is not a multiple of the number of SMs, the
  * last wave runs on part of the GPU only; stream-K splits the remaining work
  * over all CTAs along K.  Here all full waves but the last run data-parallel
- * (one 128 x 256 tile per CTA, or per CTA pair, at a time); the k blocks of
- * the remaining tiles are divided into one equal contiguous range per
- * worker.  With fewer single-CTA tiles than SMs and a long K (M > 64, when
- * the ranges come out at least 32 k blocks shorter than a tile and the
- * operand that several tiles share fits in half of L2), all tiles are spread
- * this way over up to two CTAs per tile.  A tile cut between workers is
+ * (one 128 x 256 tile per CTA, or a 256 x 256 tile per CTA pair, at a time);
+ * the k blocks of the remaining tiles are divided into one equal contiguous
+ * range per worker.  That applies only when the plain schedule's partial last
+ * wave would idle long enough to pay for the cut tiles' fix-up: (ceil(W) - W)
+ * times the k blocks of a tile at least 40, for W = tiles / workers.  With
+ * fewer single-CTA tiles than SMs and a long K (M > 64), each tile's k blocks
+ * are cut into k blocks / 128 + 1 equal pieces (2 to 8, pieces x tiles <= SMs)
+ * when that shortens the work of a CTA by at least 32 k blocks and the
+ * operand several tiles share fits in half of L2.  A tile cut between workers is
  * summed in fp32 before the ReLU and the fp16 store: each cut is settled by
  * whichever of its two sides gets there second, each side publishing its
  * fp32 part through `workspace` unless the other's is already there, and no
@@ -134,9 +137,8 @@ size_t gemm_relu_f16_streamk_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *            smaller than that or misaligned.  With aligned pitches but an
  *            unaligned base, the copies are made when the workspace has room
  *            for them, else gemm_relu_f16's predicated-load kernel runs.
- * When the tiles already fill whole waves and the operands' rows are
- * aligned, the call runs gemm_relu_f16's kernel and leaves the workspace
- * untouched.
+ * When no stream-K schedule applies and the operands' rows are aligned, the
+ * call runs gemm_relu_f16's kernel and leaves the workspace untouched.
  */
 int gemm_relu_f16_streamk(const void *A, const void *B, void *C,
                           int64_t M, int64_t N, int64_t K,
