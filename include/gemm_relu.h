@@ -350,8 +350,9 @@ int gemm_relu_debug_streamk(int mode);
  * gemm_relu_debug_streamk_pieces -- test hook.  The number of pieces each
  * tile's k blocks are cut into by gemm_relu_f16_streamk's sub-wave schedule
  * (fewer single-CTA tiles than SMs): 2 .. 8, or 0 for the library's choice
- * (default; 2, each tile cut once in the middle).  With 3 or more, tiles
- * have middle pieces and are settled through chains of cuts.  Affects the
+ * (default: k blocks / 128 + 1, from 2 to 8).  With 2 each tile is cut once
+ * in the middle; with 3 or more, tiles have middle pieces and are settled
+ * through chains of cuts.  Affects the
  * calling process only.  Returns GEMMRELU_OK, or GEMMRELU_ERR_INVALID_ARG
  * for another value.
  */
